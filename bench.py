@@ -1,0 +1,574 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the quantized paged KV path on GB300.
+
+One step = one decode step through every layer of the workload's model.  Each
+layer runs kvq_append (quantize the new token's K/V row into its page) and
+kvq_decode_attention (or kvq_window_decode) over the layer's whole cache.  The
+layers' caches together are larger than L2, so each layer's KV comes from HBM
+on every step.  The step is captured once in a CUDA graph and replayed.
+
+Printed (rank 0, one JSON line): decode-attention KV GB/s for the whole job
+(algorithmic bytes / step time), query and context tokens/s, the roofline of
+the decode call (its average duration from CUDA events recorded inside the
+graph), the end-to-end number through host buffers, clocks seen during the
+timed region, and the CPU oracle timed on a bounded sample of the same work.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...      # the CPU oracle as the reference arm
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import kvq_workloads as wl  # noqa: E402
+
+METRIC = "decode-attention KV GB/s and % of HBM peak; attention tokens/s at 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+
+# Layers of each model: (workload, number of layers, window decode?)
+MODELS = {
+    "llama8b": [("llama8b", 32, False)],                       # Llama-3.1-8B: 32 layers
+    "contbatch": [("contbatch", 1, False)],                    # 1.16 GB per layer already > L2
+    "long_mixed": [("long_mixed", 4, False)],
+    "gemma_mix": [("gemma_mix", 25, True), ("gemma_mix", 5, False)],   # 25 window + 5 global
+}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def algorithmic_bytes(w: dict, lens: np.ndarray, window: int) -> tuple[int, int]:
+    """(decode-call bytes, append-call bytes) the method must move.
+
+    Decode: K/V codes and scales of every attended token, q, out, the block-table
+    entries it reads and seq_lens.  Append: the new K/V rows, the RoPE row,
+    positions, and the codes and scales written.  Per-token sizes come from the
+    library's kvq_cache_bytes.
+    """
+    from int8_quantized_paged_gb300 import kvq
+    hd, hkv, hq = w["head_dim"], w["n_kv_heads"], w["n_heads"]
+    act = 4 if w["act"] == "f32" else 2
+    per_tok = kvq.cache_bytes(kvq.config(**w), 1, 16) // (16 * hkv)     # K + V bytes per token-head
+    att = np.minimum(lens, window) if window else lens
+    B = len(lens)
+    dec = int(att.sum()) * hkv * per_tok + 2 * B * hq * hd * act + 4 * int(np.ceil(att / 16).sum()) + 4 * B
+    app = B * (2 * hkv * hd * act + 4 * hd + 8 + hkv * per_tok)
+    return dec, app
+
+
+def load_peaks() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class _Cu:
+    """Driver-API events that can be recorded as graph nodes (external records)."""
+
+    def __init__(self):
+        self.lib = ctypes.CDLL("libcuda.so.1")
+        self.lib.cuEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint]
+        self.lib.cuEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.lib.cuEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        self.lib.cuEventDestroy_v2.argtypes = [ctypes.c_void_p]
+
+    def event(self):
+        e = ctypes.c_void_p()
+        r = self.lib.cuEventCreate(ctypes.byref(e), 0)
+        if r != 0:
+            raise RuntimeError(f"cuEventCreate failed: {r}")
+        return e
+
+    def record_external(self, ev, stream_handle: int):
+        r = self.lib.cuEventRecordWithFlags(ev, ctypes.c_void_p(stream_handle), 1)  # CU_EVENT_RECORD_EXTERNAL
+        if r != 0:
+            raise RuntimeError(f"cuEventRecordWithFlags failed: {r}")
+
+    def elapsed_ms(self, a, b) -> float:
+        ms = ctypes.c_float()
+        r = self.lib.cuEventElapsedTime(ctypes.byref(ms), a, b)
+        if r != 0:
+            raise RuntimeError(f"cuEventElapsedTime failed: {r}")
+        return ms.value
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv") \
+            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/kvq_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest value over all ranks (every rank gets it)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Units per second for the whole job: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / (ms_max / 1e3)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+
+class BenchLayer:
+    def __init__(self, w: dict, window: bool, layer: int, device, gen):
+        import torch
+        from int8_quantized_paged_gb300 import kvq
+        from int8_quantized_paged_gb300.cache import LayerCache
+        self.w = w
+        self.lens = wl.seq_lens(w)
+        self.B = len(self.lens)
+        self.window = int(w["window"]) if window else 0
+        self.ring = int(w["ring_rows"]) if window else 0
+        cfg = kvq.config(**w)
+        P = 16
+        if self.ring:
+            max_pages = self.ring // P
+            n_pages = self.B * max_pages
+        else:
+            max_pages = int(math.ceil(self.lens.max() / P))
+            n_pages = int(sum(math.ceil(L / P) for L in self.lens))
+        pool = kvq.Pool(n_pages)
+        if w.get("shuffle_pages"):
+            pool.alloc(n_pages)
+            pool.free(wl.page_free_order(w, n_pages))
+        rope_max = int(self.lens.max()) + 1
+        self.cache = LayerCache(cfg, self.B, max_pages, n_pages, rope_max, self.ring, device=device, pool=pool)
+        for b, L in enumerate(self.lens):
+            self.cache.reserve(b, self.ring if self.ring else int(L))
+        self.cache.sync_table()
+        act = self.cache.act_dtype
+        hkv, hd, hq = w["n_kv_heads"], w["head_dim"], w["n_heads"]
+
+        def rows(n):
+            x = torch.randn((n, hkv, hd), generator=gen, device=device, dtype=torch.float32)
+            if w.get("outlier_frac", 0):
+                m = torch.rand((n, hkv, hd), generator=gen, device=device) < w["outlier_frac"]
+                x = torch.where(m, x * 8, x)
+            return x.to(act)
+
+        # Prefill every sequence (the product's append path, chunked so no call
+        # writes one ring row twice).
+        for b, L in enumerate(self.lens):
+            step = self.ring if self.ring else int(L)
+            for s in range(0, int(L), step):
+                e = min(int(L), s + step)
+                self.cache.append(rows(e - s), rows(e - s),
+                                  torch.arange(s, e, dtype=torch.int32, device=device),
+                                  torch.full((e - s,), b, dtype=torch.int32, device=device))
+        # This step's inputs: the token at position L-1 of every sequence.
+        self.q = torch.randn((self.B, hq, hd), generator=gen, device=device).to(act)
+        self.k_new, self.v_new = rows(self.B), rows(self.B)
+        self.pos = torch.from_numpy(self.lens - 1).to(device)
+        self.seq_lens = torch.from_numpy(self.lens).to(device)
+        self.out = torch.empty_like(self.q)
+        self.ws = self.cache.workspace(self.B, 0, self.window)
+        self.dec_bytes, self.app_bytes = algorithmic_bytes(w, self.lens, self.window)
+
+    def append(self):
+        self.cache.append(self.k_new, self.v_new, self.pos)
+
+    def decode(self):
+        if self.window:
+            self.cache.window_decode(self.q, self.seq_lens, self.out, self.ws, self.window)
+        else:
+            self.cache.decode(self.q, self.seq_lens, self.out, self.ws)
+
+
+def run_gpu(args) -> dict | None:
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    from int8_quantized_paged_gb300 import build as _build
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    from int8_quantized_paged_gb300 import kvq
+
+    layers = []
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + 97 * rank)
+    for name, n, window in MODELS[args.workload]:
+        w = wl.workload(name)
+        for i in range(n):
+            layers.append(BenchLayer(w, window, len(layers), dev, gen))
+    torch.cuda.synchronize()
+    for L in layers:
+        assert L.cache.status_bits() == 0, "prefill flagged a bad page or position"
+
+    step_bytes = sum(L.dec_bytes + L.app_bytes for L in layers)
+    query_tokens = layers[0].B
+    ctx_tokens = sum(int((np.minimum(L.lens, L.window) if L.window else L.lens).sum()) for L in layers)
+
+    stream = torch.cuda.Stream(device=dev)
+    cu = _Cu()
+
+    def step():
+        for L in layers:
+            L.append()
+            L.decode()
+
+    # warm up outside capture, then capture the step (graph A) and the step with
+    # external event records around every decode call (graph B).
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    g_a = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_a, stream=stream):
+        step()
+    evs = [(cu.event(), cu.event()) for _ in layers]
+    g_b = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_b, stream=stream):
+        for L, (e0, e1) in zip(layers, evs):
+            L.append()
+            cu.record_external(e0, torch.cuda.current_stream().cuda_stream)
+            L.decode()
+            cu.record_external(e1, torch.cuda.current_stream().cuda_stream)
+    launches_per_step = 3 * len(layers)   # append, split-K decode, combine
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_a.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(args.steps):
+            g_a.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = t0.elapsed_time(t1) / args.steps
+
+    # decode-call durations: graph B, one step per replay
+    dec_ms = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            g_b.replay()
+            stream.synchronize()
+            dec_ms.extend(cu.elapsed_ms(e0, e1) for e0, e1 in evs)
+    torch.cuda.synchronize()
+
+    # end to end: pinned host inputs -> device, the step, outputs -> pinned host
+    h_in = [[t.cpu().pin_memory() for t in (L.q, L.k_new, L.v_new)] for L in layers]
+    h_out = [L.out.cpu().pin_memory() for L in layers]
+    h2d = sum(t.numel() * t.element_size() for ts in h_in for t in ts)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            for L, (hq, hk, hv) in zip(layers, h_in):
+                L.q.copy_(hq, non_blocking=True)
+                L.k_new.copy_(hk, non_blocking=True)
+                L.v_new.copy_(hv, non_blocking=True)
+            g_a.replay()
+            for L, ho in zip(layers, h_out):
+                ho.copy_(L.out, non_blocking=True)
+            stream.synchronize()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+    for L in layers:
+        assert L.cache.status_bits() == 0, "a kernel flagged a bad page, position or length"
+
+    ms_max = max_over_ranks(ms, world)
+    e2e_max = max_over_ranks(e2e_ms, world)
+    dec_avg = statistics.mean(dec_ms)
+    dec_bytes = statistics.mean(L.dec_bytes for L in layers)
+    peak, peak_kind = load_peaks()
+    achieved = dec_bytes / (dec_avg / 1e3) / 1e9
+    value = whole_job(step_bytes, world, ms_max) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int4/int8 codes, fp32 math",
+        "data": "synthetic: seeded N(0,1) activations of the workload's shapes; no model weights",
+        "config": {
+            "workload": args.workload,
+            "layers": len(layers),
+            "batch": layers[0].B,
+            "ctx": int(layers[0].lens.max()),
+            "kv_bytes_per_step": step_bytes,
+            "l2": "inputs larger than L2: %d layer caches of %.1f MB each are read in turn"
+                  % (len(layers), dec_bytes / 1e6),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "graph": "CUDA graph of one step",
+        },
+        "tokens_per_s": round(whole_job(query_tokens, world, ms_max), 1),
+        "context_tokens_per_s": round(whole_job(ctx_tokens, world, ms_max), 1),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "kvq_decode_attention (split-K decode + combine)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": None,
+            "algorithmic_bytes_per_launch": int(dec_bytes),
+            "avg_launch_us": round(dec_avg * 1e3, 3),
+            "median_launch_us": round(statistics.median(dec_ms) * 1e3, 3),
+        },
+        "e2e": {
+            "value": round(whole_job(step_bytes, world, e2e_max) / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_max, 5),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    return res if rank == 0 else None
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample(workload: str):
+    """One bounded unit of the workload for the CPU oracle: the first layer of the
+    model with its cache filled by the oracle's own append (set-up, untimed).  For
+    the continuous batch the sample is its first 4 sequences."""
+    from oracle import kvq_oracle as O
+    name, _, window = MODELS[workload][0]
+    w = wl.workload(name)
+    lens = wl.seq_lens(w)
+    if workload == "contbatch":
+        lens = lens[:4]
+    spec = O.Spec.from_workload(w)
+    ring = int(w["ring_rows"]) if window else 0
+    win = int(w["window"]) if window else 0
+    P = 16
+    maxp = ring // P if ring else int(math.ceil(lens.max() / P))
+    bt = np.arange(len(lens) * maxp, dtype=np.int32).reshape(len(lens), maxp)
+    pools = {"k": np.zeros(bt.size * O.page_bytes(spec, "k"), np.uint8),
+             "v": np.zeros(bt.size * O.page_bytes(spec, "v"), np.uint8)}
+    tab = O.rope_table(spec.head_dim, spec.rope_base, int(lens.max()) + 1)
+    for b, L in enumerate(lens):
+        k, v = wl.kv_rows(w, b, "k", int(L)), wl.kv_rows(w, b, "v", int(L))
+        O.append(spec, pools, k, v, np.full(int(L), b), np.arange(int(L)), bt, ring, tab)
+    q = wl.queries(dict(w, batch=len(lens)))
+    knew = wl.new_rows(w, "k", len(lens))
+    vnew = wl.new_rows(w, "v", len(lens))
+    dec, app = algorithmic_bytes(w, lens, win)
+
+    def step():
+        O.append(spec, pools, knew, vnew, np.arange(len(lens)), lens - 1, bt, ring, tab)
+        O.decode(spec, q, pools, bt, lens, win, ring)
+
+    desc = (f"oracle append + decode of 1 {name} layer ({len(lens)} seq, "
+            f"{int((np.minimum(lens, win) if win else lens).sum())} attended tokens), "
+            f"cache filled by the oracle untimed")
+    return step, dec + app, desc
+
+
+def cpu_worker(workload: str, seconds: float, steps: int, warmup: int) -> dict:
+    step, nbytes, desc = oracle_sample(workload)
+    for _ in range(warmup):
+        step()
+    times = []
+    t_end = time.perf_counter() + seconds
+    while (steps and len(times) < steps) or (not steps and (time.perf_counter() < t_end or not times)):
+        t = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t)
+    mean = sum(times) / len(times)
+    return {"value": round(nbytes / mean / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{desc}; {len(times)} timed calls, {mean * 1e3:.1f} ms each",
+            "ms_per_step": mean * 1e3}
+
+
+def run_cpu_worker_subprocess(workload: str, seconds: float, steps: int = 0, warmup: int = 1) -> dict:
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--workload", workload,
+           "--cpu-seconds", str(seconds), "--steps", str(steps), "--warmup", str(warmup)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError(f"cpu worker failed:\n{r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    r = run_cpu_worker_subprocess(args.workload, 0.0, steps=args.steps, warmup=args.warmup)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": r["value"],
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(r["ms_per_step"], 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (codes in fp32)",
+        "data": "synthetic: seeded N(0,1) activations of the workload's shapes; no model weights",
+        "config": {"workload": args.workload, "sample": r["sample"]},
+        "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--workload", choices=list(MODELS), default="llama8b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.cpu_worker and args.impl == "kvq":
+        ap.error("--warmup must be >= 3")
+
+    if args.cpu_worker:
+        print(json.dumps(cpu_worker(args.workload, args.cpu_seconds, args.steps, args.warmup)))
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    res = run_gpu(args)
+    rank, world, _ = dist_env()
+    if res is not None:
+        if world == 1 and not args.no_cpu_baseline:
+            cb = run_cpu_worker_subprocess(args.workload, args.cpu_seconds)
+            cb.pop("ms_per_step", None)
+            res["cpu_baseline"] = cb
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+"""GPU path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Codes and scales: bytewise equal pools.  Outputs: max row-relative error
+<= 2e-3 (elements below 1e-3 of the row's largest magnitude compare against
+that floor).  Sizes span several chunks, several pages and ragged tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kvq_workloads as wl
+from gpu_cases import TOL, Case, max_row_err
+from int8_quantized_paged_gb300 import kvq
+
+pytestmark = pytest.mark.gpu
+
+needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    torch.cuda.init()
+
+
+SMALL = {
+    "tiny": dict(lens=[256]),
+    "llama8b": dict(lens=[1000, 37, 2049], over=dict(batch=3)),
+    "contbatch": dict(lens=[0, 1, 16, 17, 700, 2900], over=dict(batch=6)),
+    "gemma_mix": dict(lens=[3001, 5], over=dict(batch=2)),
+    "long_mixed": dict(lens=[5000, 777], over=dict(batch=2)),
+}
+
+
+def _case(name, **kw):
+    spec = SMALL[name]
+    w = wl.workload(name, **spec.get("over", {}))
+    return Case(w, spec["lens"], **kw)
+
+
+@pytest.fixture(scope="module", params=list(SMALL))
+def case(request):
+    return _case(request.param)
+
+
+def test_append_codes_bytewise(case):
+    k, v = case.gpu_pools()
+    assert np.array_equal(k, case.pools["k"])
+    assert np.array_equal(v, case.pools["v"])
+    assert case.cache.status_bits() == 0
+
+
+@pytest.mark.parametrize("chunk", [0, 16, 64, 512])
+def test_decode_matches_oracle(case, chunk):
+    q = case.queries()
+    ref = case.oracle_decode(q)
+    got = case.gpu_decode(q, chunk_tokens=chunk)
+    assert np.all(np.isfinite(got))
+    assert max_row_err(got, ref) <= TOL
+    for b, L in enumerate(case.lens):
+        if L == 0:
+            assert np.all(got[b] == 0)
+    assert case.cache.status_bits() == 0
+
+
+def test_chunk_count_invariance(case):
+    q = case.queries(step=1)
+    a = case.gpu_decode(q, chunk_tokens=16)
+    b = case.gpu_decode(q, chunk_tokens=1024)
+    c = case.gpu_decode(q)
+    ref = case.oracle_decode(q)
+    for x in (a, b, c):
+        assert max_row_err(x, ref) <= TOL
+    assert np.max(np.abs(a - c)) <= 4e-3 * max(1e-6, np.max(np.abs(ref)))
+
+
+@pytest.mark.parametrize("L", [1, 1000, 1024, 1025, 1152, 1153, 3000])
+def test_window_ring_matches_oracle(L):
+    w = wl.workload("gemma_mix")
+    c = Case(w, [L], ring_rows=1152)
+    k, v = c.gpu_pools()
+    assert np.array_equal(k, c.pools["k"]) and np.array_equal(v, c.pools["v"])
+    q = c.queries()
+    ref = c.oracle_decode(q, window=1024)
+    for chunk in (0, 64):
+        got = c.gpu_decode(q, chunk_tokens=chunk, window=1024)
+        assert max_row_err(got, ref) <= TOL, (L, chunk)
+
+
+def test_window_small_ring_other_codec():
+    # a symmetric-INT4 layer with a 64-row ring and a 40-token window
+    w = wl.workload("llama8b", batch=3)
+    c = Case(w, [10, 64, 333], ring_rows=64)
+    q = c.queries()
+    ref = c.oracle_decode(q, window=40)
+    got = c.gpu_decode(q, window=40)
+    assert max_row_err(got, ref) <= TOL
+
+
+def test_length_one_returns_its_value():
+    w = wl.workload("llama8b", batch=1)
+    c = Case(w, [1])
+    q = c.queries()
+    got = c.gpu_decode(q)
+    ref = c.oracle_decode(q)                       # = the dequantized v of token 0
+    assert max_row_err(got, ref) <= TOL
+
+
+def test_non_default_stream_and_isolation():
+    w = wl.workload("llama8b", batch=2)
+    c = Case(w, [300, 500], extra_pages=4)
+    q = c.queries()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        before = c.gpu_decode(q, stream=s)
+    ref = c.oracle_decode(q)
+    assert max_row_err(before, ref) <= TOL
+    # grow sequence 0 by one token: sequence 1's output must not change at all
+    c.cache.reserve(0, 301)
+    c.cache.sync_table()
+    dev = c.cache.device
+    rows = torch.from_numpy(wl.new_rows(w, "k", 1)).to(dev)
+    c.cache.append(rows, rows, torch.tensor([300], dtype=torch.int32, device=dev),
+                   torch.tensor([0], dtype=torch.int32, device=dev))
+    after = c.gpu_decode(q, lens=[301, 500])
+    assert np.array_equal(before[1], after[1])
+    assert not np.array_equal(before[0], after[0])
+
+
+def test_device_status_flags_bad_inputs():
+    w = wl.workload("llama8b", batch=3)
+    c = Case(w, [40, 40, 40], fill_oracle=True)
+    q = c.queries()
+    ref = c.oracle_decode(q)
+    dev = c.cache.device
+    # a page id outside the pool in sequence 1
+    bad = c.bt.copy()
+    bad[1, 1] = c.n_pages + 5
+    c.cache.set_table(bad)
+    kvq.clear_device_status(c.cache.status)
+    got = c.gpu_decode(q)
+    assert c.cache.status_bits() & kvq.DEV_BAD_PAGE
+    assert max_row_err(got, ref, seqs=[0, 2]) <= TOL         # other sequences unaffected
+    c.cache.set_table(c.bt)
+    # a length past the table's capacity gives a zero row and a flag
+    kvq.clear_device_status(c.cache.status)
+    got = c.gpu_decode(q, lens=[40, 10 ** 6, 40])
+    assert c.cache.status_bits() & kvq.DEV_BAD_LEN
+    assert np.all(got[1] == 0) and max_row_err(got, ref, seqs=[0, 2]) <= TOL
+    # append: a sequence id and a position outside the table are flagged and skipped
+    kvq.clear_device_status(c.cache.status)
+    k0 = c.cache.k_pool.clone()
+    rows = torch.zeros(2, 8, 128, dtype=torch.float16, device=dev)
+    c.cache.append(rows, rows, torch.tensor([5, 10 ** 5], dtype=torch.int32, device=dev),
+                   torch.tensor([7, 0], dtype=torch.int32, device=dev))
+    bits = c.cache.status_bits()
+    assert bits & kvq.DEV_BAD_SEQ and bits & kvq.DEV_BAD_POS
+    assert torch.equal(k0, c.cache.k_pool)
+    kvq.clear_device_status(c.cache.status)
+    assert c.cache.status_bits() == 0
+
+
+def test_empty_batch_is_noop():
+    w = wl.workload("tiny")
+    c = Case(w, [256], fill_oracle=False)
+    cfg = c.cfg
+    q = torch.zeros(0, 4, 64, dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    kvq.decode_attention(cfg, q, c.cache.k_pool, c.cache.v_pool, c.n_pages, c.cache.block_table,
+                         c.max_pages, c.cache.block_table, c.cache.rope_tab, c.rope_max, q, ws, c.cache.status)
