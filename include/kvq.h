@@ -3,9 +3,10 @@
  *
  * C ABI of libkvq.so.  Plain pointers and sizes only.  Every device buffer
  * (pools, block tables, q, out, workspace, status word) is allocated and owned
- * by the caller.  The library does not allocate device memory on any path.
- * The host-side page pool and block-table objects are the only allocations it
- * makes, and they live in host memory.
+ * by the caller.  The library never calls a device allocator.  Its only device
+ * memory of its own is the fixed scratch array behind
+ * kvq_decode_attention_noalloc.  The host-side page pool and block-table
+ * objects are the only allocations it makes, and they live in host memory.
  *
  * The method restated here comes from four web pages:
  *   [Shimmy]    "Shimmy 深度解剖：Airframe 引擎与 TurboShimmy INT4 KV"
@@ -271,6 +272,31 @@ kvq_status kvq_window_decode(const kvq_config* cfg, int32_t batch, const void* q
                              const float* rope_tab, int32_t rope_max_pos,
                              void* out, void* workspace, size_t workspace_bytes,
                              int32_t chunk_tokens, int32_t* dev_status, kvq_stream_t stream);
+
+/* ------------------------------------------- decode without allocation --
+ * The pages have no counterpart to this entry point.  It exists for callers
+ * that cannot allocate device memory, such as a plugin whose host engine owns
+ * all of HBM through its own pool, or a hot path where an allocation and the
+ * synchronization it may cause are not allowed.
+ * It computes exactly what kvq_decode_attention computes, with the same
+ * arguments minus the workspace.  The split-K workspace is a fixed
+ * KVQ_NOALLOC_SCRATCH_BYTES array compiled into the library.  Every GPU that
+ * loads the library holds that array until the process exits.  A decode whose
+ * workspace (kvq_decode_workspace_bytes) is larger returns
+ * KVQ_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current, so make that first call before any stream capture.  All calls share
+ * the one array: calls whose kernels overlap on the GPU (for example on two
+ * streams at once) race.  The library neither allocates nor frees memory here,
+ * and the array needs no clearing between calls. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)   /* 8 MiB */
+kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, int32_t batch, const void* q,
+                                        const void* k_pool, const void* v_pool, int32_t n_pool_pages,
+                                        const int32_t* block_table, int32_t max_pages_per_seq,
+                                        const int32_t* seq_lens,
+                                        const float* rope_tab, int32_t rope_max_pos,
+                                        void* out, int32_t chunk_tokens, int32_t* dev_status,
+                                        kvq_stream_t stream);
 
 /* ---------------------------------------------------------- device status --
  * Clear the status word (an async memset on stream). */

@@ -84,6 +84,8 @@ _SIGS = {
     "kvq_window_workspace_bytes": (_sz, [_cfgp, _i32, _i32, _i32]),
     "kvq_window_decode": (C.c_int, [_cfgp, _i32, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp, _vp,
                                     _i32, _vp, _vp, _sz, _i32, _vp, _vp]),
+    "kvq_decode_attention_noalloc": (C.c_int, [_cfgp, _i32, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp,
+                                               _i32, _vp, _i32, _vp, _vp]),
     "kvq_clear_device_status": (C.c_int, [_vp, _vp]),
     "kvq_get_device_status": (C.c_int, [_vp, _vp, C.POINTER(_i32)]),
 }
@@ -265,6 +267,19 @@ def decode_attention(cfg: Config, q, k_pool, v_pool, n_pool_pages: int, block_ta
         C.byref(cfg), q.shape[0], _ptr(q), _ptr(k_pool), _ptr(v_pool), n_pool_pages, _ptr(block_table),
         max_pages_per_seq, _ptr(seq_lens), _ptr(rope_tab), rope_max_pos, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), chunk_tokens, _ptr(dev_status), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def decode_attention_noalloc(cfg: Config, q, k_pool, v_pool, n_pool_pages: int, block_table,
+                             max_pages_per_seq: int, seq_lens, rope_tab, rope_max_pos: int, out,
+                             dev_status, chunk_tokens: int = 0, stream=None) -> None:
+    """kvq_decode_attention with the library's built-in scratch as workspace."""
+    _check(lib().kvq_decode_attention_noalloc(
+        C.byref(cfg), q.shape[0], _ptr(q), _ptr(k_pool), _ptr(v_pool), n_pool_pages, _ptr(block_table),
+        max_pages_per_seq, _ptr(seq_lens), _ptr(rope_tab), rope_max_pos, _ptr(out), chunk_tokens,
+        _ptr(dev_status), _stream(stream)))
 
 
 def window_workspace_bytes(cfg: Config, batch: int, window: int, chunk_tokens: int = 0) -> int:
