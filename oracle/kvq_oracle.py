@@ -512,6 +512,14 @@ def decode(spec: Spec, q: np.ndarray, pools: dict, block_table: np.ndarray,
     return out
 
 
+def row_norm_error(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """Per (b, h) row: max_i |got_i - ref_i| / max_i |ref_i| (normwise)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.max(np.abs(ref), axis=-1)
+    return np.max(np.abs(got - ref), axis=-1) / np.where(den == 0, 1.0, den)
+
+
 def decode_contiguous(spec: Spec, q: np.ndarray, k_rows: list, v_rows: list,
                       seq_lens, rope_tab, window: int = 0) -> np.ndarray:
     """Same result computed without pages: quantise each sequence's rows in
@@ -538,8 +546,13 @@ def decode_contiguous(spec: Spec, q: np.ndarray, k_rows: list, v_rows: list,
 # Comparison rule for fp outputs
 
 
-def row_rel_error(got: np.ndarray, ref: np.ndarray, floor: float = 1e-3) -> np.ndarray:
-    """Per (b, h) row: max_i |got_i - ref_i| / max(|ref_i|, floor * max|ref_row|)."""
+def row_rel_error(got: np.ndarray, ref: np.ndarray, floor: float = 1e-2) -> np.ndarray:
+    """Per (b, h) row: max_i |got_i - ref_i| / max(|ref_i|, floor * max|ref_row|).
+
+    Reading of "max relative error" on the output: elements within 100x of the
+    row's largest magnitude are compared relatively; smaller ones against 1 %
+    of that magnitude, since their own relative error is ill-conditioned.
+    """
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     rmax = np.max(np.abs(ref), axis=-1, keepdims=True)

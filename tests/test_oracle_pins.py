@@ -420,5 +420,8 @@ def test_row_rel_error_rule():
     assert O.row_rel_error(ref, ref)[0] == 0
     got = ref + np.array([[1e-3, 0, 0, 0]])
     assert math.isclose(O.row_rel_error(got, ref)[0], 1e-3)
-    got = ref + np.array([[0, 0, 1e-6, 0]])                # near-zero element uses the row floor
+    got = ref + np.array([[0, 0, 1e-5, 0]])                # near-zero element uses the row floor (1 %)
     assert math.isclose(O.row_rel_error(got, ref)[0], 1e-3)
+    got = ref + np.array([[0, 2e-4, 0, 0]])                # 0.5 is above the floor: relative to itself
+    assert math.isclose(O.row_rel_error(got, ref)[0], 4e-4)
+    assert math.isclose(O.row_norm_error(got, ref)[0], 2e-4)
