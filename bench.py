@@ -202,7 +202,7 @@ def whole_job(units_per_rank: float, world: int, ms_max: float) -> float:
 
 
 class BenchLayer:
-    def __init__(self, w: dict, window: bool, layer: int, device, gen):
+    def __init__(self, w: dict, window: bool, layer: int, device, gen, chunk_tokens: int = 0):
         import torch
         from int8_quantized_paged_gb300 import kvq
         from int8_quantized_paged_gb300.cache import LayerCache
@@ -253,7 +253,8 @@ class BenchLayer:
         self.pos = torch.from_numpy(self.lens - 1).to(device)
         self.seq_lens = torch.from_numpy(self.lens).to(device)
         self.out = torch.empty_like(self.q)
-        self.ws = self.cache.workspace(self.B, 0, self.window)
+        self.chunk = chunk_tokens
+        self.ws = self.cache.workspace(self.B, chunk_tokens, self.window)
         self.dec_bytes, self.app_bytes = algorithmic_bytes(w, self.lens, self.window)
 
     def append(self):
@@ -261,9 +262,9 @@ class BenchLayer:
 
     def decode(self):
         if self.window:
-            self.cache.window_decode(self.q, self.seq_lens, self.out, self.ws, self.window)
+            self.cache.window_decode(self.q, self.seq_lens, self.out, self.ws, self.window, self.chunk)
         else:
-            self.cache.decode(self.q, self.seq_lens, self.out, self.ws)
+            self.cache.decode(self.q, self.seq_lens, self.out, self.ws, self.chunk)
 
 
 def run_gpu(args) -> dict | None:
@@ -284,7 +285,7 @@ def run_gpu(args) -> dict | None:
     for name, n, window in MODELS[args.workload]:
         w = wl.workload(name)
         for i in range(n):
-            layers.append(BenchLayer(w, window, len(layers), dev, gen))
+            layers.append(BenchLayer(w, window, len(layers), dev, gen, args.chunk_tokens))
     torch.cuda.synchronize()
     for L in layers:
         assert L.cache.status_bits() == 0, "prefill flagged a bad page or position"
@@ -405,6 +406,7 @@ def run_gpu(args) -> dict | None:
                   % (len(layers), dec_bytes / 1e6),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "graph": "CUDA graph of one step",
+            "chunk_tokens": args.chunk_tokens or "library default",
         },
         "tokens_per_s": round(whole_job(query_tokens, world, ms_max), 1),
         "context_tokens_per_s": round(whole_job(ctx_tokens, world, ms_max), 1),
@@ -543,6 +545,8 @@ def main():
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     ap.add_argument("--workload", choices=list(MODELS), default="llama8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunk-tokens", type=int, default=0,
+                    help="tokens per split-K chunk (0: the library chooses)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()

@@ -85,6 +85,7 @@ typedef enum kvq_status {
 #define KVQ_DEV_BAD_POS 2         /* a position past the block table or the RoPE table */
 #define KVQ_DEV_BAD_SEQ 4         /* a sequence id outside [0, n_seqs) */
 #define KVQ_DEV_BAD_LEN 8         /* a seq_len < 0 or past the block table's capacity */
+#define KVQ_DEV_TIMEOUT 16        /* a bounded wait on a copy gave up (should never happen) */
 
 typedef enum kvq_float { KVQ_F32 = 0, KVQ_F16 = 1, KVQ_BF16 = 2 } kvq_float;
 
@@ -233,14 +234,18 @@ kvq_status kvq_append(const kvq_config* cfg, int32_t n_rows,
  *   s_t = alpha * <q~, K^_t>  for t in [0, L)
  *   out[b][h] = sum_t softmax(s)_t V^_t      (L = 0 gives zeros)
  * The context is split into chunks of chunk_tokens tokens.  Each chunk keeps an
- * fp32 online softmax (m, l, acc), and a second kernel combines the chunks
- * with log-sum-exp weights.  fp32 softmax: [airllm] §3.4.
+ * fp32 online softmax (m, l, acc), and the last chunk of each (sequence, kv
+ * head) to finish merges the chunks with log-sum-exp weights.  fp32 softmax:
+ * [airllm] §3.4.
  *   q, out        device [batch][n_heads][head_dim] of act_dtype
  *   seq_lens      device int32 [batch], 0 <= L <= max_pages_per_seq*page_size
  *   chunk_tokens  0: the library chooses; else a multiple of page_size
  *   workspace     device scratch of at least kvq_decode_workspace_bytes()
  *                 with the same batch, max_pages_per_seq and chunk_tokens;
- *                 256-byte aligned; its contents need no initialisation
+ *                 256-byte aligned.  Zero it once before its first use: its
+ *                 first bytes are per-(sequence, kv head) arrival counters,
+ *                 and every completed call leaves them zero again.  Zero it
+ *                 again before using it for a larger batch.
  * A sequence whose length is bad sets KVQ_DEV_BAD_LEN and gets a zero row.  A
  * bad page id sets KVQ_DEV_BAD_PAGE and its tokens are left out. */
 size_t kvq_decode_workspace_bytes(const kvq_config* cfg, int32_t batch,
@@ -287,8 +292,9 @@ kvq_status kvq_window_decode(const kvq_config* cfg, int32_t batch, const void* q
  * looks up the array's device address (cudaGetSymbolAddress) with that device
  * current, so make that first call before any stream capture.  All calls share
  * the one array: calls whose kernels overlap on the GPU (for example on two
- * streams at once) race.  The library neither allocates nor frees memory here,
- * and the array needs no clearing between calls. */
+ * streams at once) race.  The library neither allocates nor frees memory here.
+ * The array starts zeroed when the library loads, and every completed call
+ * leaves its arrival counters zero again, so nothing needs clearing. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)   /* 8 MiB */
 kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, int32_t batch, const void* q,
                                         const void* k_pool, const void* v_pool, int32_t n_pool_pages,

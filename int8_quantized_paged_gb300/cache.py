@@ -58,7 +58,7 @@ class LayerCache:
             n = kvq.window_workspace_bytes(self.cfg, batch, window, chunk_tokens)
         else:
             n = kvq.decode_workspace_bytes(self.cfg, batch, self.max_pages, chunk_tokens)
-        return torch.empty(n, dtype=torch.uint8, device=self.device)
+        return torch.zeros(n, dtype=torch.uint8, device=self.device)   # counters start at zero
 
     def decode(self, q, seq_lens, out, workspace, chunk_tokens: int = 0, stream=None) -> None:
         kvq.decode_attention(self.cfg, q, self.k_pool, self.v_pool, self.n_pool_pages, self.block_table,

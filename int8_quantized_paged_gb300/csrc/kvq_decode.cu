@@ -1,32 +1,139 @@
-// Decode entry points: argument checks, workspace layout, the split-K launch
-// and the log-sum-exp combine of the chunks.
+// Decode entry points: argument checks, the chunk plan and workspace layout,
+// tensor-map encoding and the launches.
+//
+// Two kernels compute the same decode.  The tensor-core kernel
+// (kvq_decode_tc.cuh) is the default.  It fuses the log-sum-exp combine into
+// the last CTA of each (sequence, kv head), so a call is one launch.  The
+// CUDA-core kernel (kvq_decode_impl.cuh) covers shapes the tensor-core kernel
+// does not take: groups that are not a multiple of 32, and 8-bit rows longer
+// than 128 bytes.  It is followed by a separate combine kernel.  Setting
+// KVQ_DECODE_IMPL=simt in the environment selects it for every shape, so the
+// two can be compared side by side.
 //
 // Combine: for chunks c with partial state (m_c, l_c, acc_c) in base 2,
 //   M = max_c m_c ;  out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c,
 // which equals the softmax over the whole context (the chunks partition it).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "kvq_decode_impl.cuh"
+#include "kvq_decode_tc.cuh"
 
 namespace kvq {
 
 static constexpr int kMaxChunks = 8192;
 
-struct WsLayout {
-  int chunk_tokens, n_chunks;
-  size_t acc_bytes, ml_offset, total;
+// Whether the tensor-core kernel takes this config (and is not switched off):
+// power-of-two groups of at least 32 elements, code rows of 32..128 bytes, and
+// one stored type for the K and V scales.
+static bool tc_enabled(const kvq_config& c) {
+  static int forced = -1;
+  if (forced < 0) {
+    const char* e = std::getenv("KVQ_DECODE_IMPL");
+    forced = (e && std::strcmp(e, "simt") == 0) ? 0 : 1;
+  }
+  if (!forced) return false;
+  const int krb = c.k_dtype == KVQ_SYM_INT8 ? c.head_dim : c.head_dim / 2;
+  const int vrb = c.v_dtype == KVQ_SYM_INT8 ? c.head_dim : c.head_dim / 2;
+  const bool pow2 = (c.k_group & (c.k_group - 1)) == 0 && (c.v_group & (c.v_group - 1)) == 0;
+  return pow2 && c.k_param_dtype == c.v_param_dtype && c.k_group >= 32 && c.v_group >= 32 && krb >= 32 && krb <= 128 && vrb >= 32 && vrb <= 128;
+}
+
+static bool pdl_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char* e = std::getenv("KVQ_PDL");
+    on = (e && std::strcmp(e, "0") == 0) ? 0 : 1;
+  }
+  return on != 0;
+}
+
+// Chunking and workspace layout of one decode call.  The workspace holds, in
+// order: arrival counters [batch][n_kv_heads] (int32, zero between calls),
+// partial sums acc [batch][n_kv_heads][n_chunks][G][head_dim] and partial
+// (max, sum) [batch][n_kv_heads][n_chunks][G][2], all fp32.  It is sized for
+// whichever kernel would run.
+struct Plan {
+  bool tc;
+  int chunk_tokens;          // CUDA-core kernel: tokens per chunk
+  int blocks_per_chunk;      // tensor-core kernel: 16-token blocks per chunk
+  int n_chunks;              // chunks per (sequence, kv head) the workspace holds
+  int tc_chunks;             // chunks the tensor-core kernel uses (grid x)
+  size_t acc_offset, ml_offset, total;
 };
 
-static WsLayout ws_layout(const kvq_config& c, int32_t batch, int64_t max_tokens, int32_t requested) {
-  WsLayout w{};
-  w.chunk_tokens = chunk_tokens_for(c, batch, max_tokens, requested);
-  w.n_chunks = (int)((max_tokens + w.chunk_tokens - 1) / w.chunk_tokens);
-  if (w.n_chunks < 1) w.n_chunks = 1;
-  const size_t units = (size_t)batch * c.n_kv_heads * w.n_chunks * (c.n_heads / c.n_kv_heads);
-  w.acc_bytes = units * c.head_dim * sizeof(float);
-  w.ml_offset = (w.acc_bytes + 255) / 256 * 256;
-  w.total = w.ml_offset + units * 2 * sizeof(float);
-  return w;
+static Plan make_plan(const kvq_config& c, int32_t batch, int64_t max_tokens, bool window, int32_t requested) {
+  Plan p{};
+  p.tc = tc_enabled(c);
+  const int P = c.page_size;
+  // CUDA-core kernel: token chunks starting at the first attended token
+  p.chunk_tokens = chunk_tokens_for(c, batch, max_tokens, requested);
+  const int64_t n_simt = (max_tokens + p.chunk_tokens - 1) / p.chunk_tokens;
+  // tensor-core kernel: page-aligned chunks; a window may start mid-page
+  const int64_t max_blocks = (max_tokens + P - 1) / P + (window ? 1 : 0);
+  if (requested > 0) {
+    p.blocks_per_chunk = requested / P;
+  } else {
+    const int64_t pairs = (int64_t)batch * c.n_kv_heads;
+    const int64_t slots = 2LL * num_sms();   // about one wave at two CTAs per SM
+    int64_t cb = (pairs * max_blocks + slots - 1) / slots;
+    const int spb = c.head_dim == 256 ? 2 : 4;   // pages per pipeline stage
+    cb = (cb + spb - 1) / spb * spb;
+    p.blocks_per_chunk = (int)(cb < 4 ? 4 : (cb > 64 ? 64 : cb));
+  }
+  if (p.blocks_per_chunk > kMaxChunkBlocks) p.tc = false;
+  const int64_t n_tc = (max_blocks + p.blocks_per_chunk - 1) / p.blocks_per_chunk;
+  p.tc_chunks = (int)(n_tc < 1 ? 1 : (n_tc > (1 << 30) ? (1 << 30) : n_tc));
+  const int64_t n = n_simt > n_tc ? n_simt : n_tc;
+  p.n_chunks = (int)(n < 1 ? 1 : (n > (1 << 30) ? (1 << 30) : n));
+  const size_t units = (size_t)batch * c.n_kv_heads * p.n_chunks * (c.n_heads / c.n_kv_heads);
+  const size_t counters = ((size_t)batch * c.n_kv_heads * sizeof(int32_t) + 255) / 256 * 256;
+  p.acc_offset = counters;
+  p.ml_offset = p.acc_offset + (units * c.head_dim * sizeof(float) + 255) / 256 * 256;
+  p.total = p.ml_offset + units * 2 * sizeof(float);
+  return p;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D tensor map over the code rows of a pool: (row bytes, 16 rows, sub-block).
+static kvq_status code_map(CUtensorMap* map, const void* pool, const PoolLayout& L, int32_t n_pool_pages,
+                           int32_t n_kv_heads) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint32_t rowb = (cuuint32_t)L.code_bytes;
+  const cuuint64_t dims[3] = {rowb, 16, (cuuint64_t)n_pool_pages * n_kv_heads};
+  const cuuint64_t strides[2] = {rowb, (cuuint64_t)L.sub_bytes};
+  const cuuint32_t box[3] = {rowb, 16, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return KVQ_OK;
 }
 
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a, void* out, int G, int HD) {
@@ -85,13 +192,13 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
                              int32_t rope_max_pos, void* out, void* workspace, size_t ws_bytes,
                              int32_t chunk_tokens, int32_t* dev_status, cudaStream_t stream,
                              int32_t ring_rows, int32_t window, int64_t max_tokens) {
-  WsLayout w = ws_layout(*cfg, batch, max_tokens, chunk_tokens);
+  const Plan w = make_plan(*cfg, batch, max_tokens, window > 0, chunk_tokens);
   if (w.n_chunks > kMaxChunks)
-    return fail(KVQ_ERR_INVALID_ARG, "%d chunks of %d tokens exceed the limit %d; use larger chunks",
-                w.n_chunks, w.chunk_tokens, kMaxChunks);
+    return fail(KVQ_ERR_INVALID_ARG, "%d chunks exceed the limit %d; use larger chunks", w.n_chunks, kMaxChunks);
   if (ws_bytes < w.total)
     return fail(KVQ_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", ws_bytes, w.total);
   if (batch == 0) return KVQ_OK;
+  if (batch > 65535 || cfg->n_kv_heads > 65535) return fail(KVQ_ERR_INVALID_ARG, "batch or n_kv_heads too large");
 
   DecodeArgs a;
   a.q = q;
@@ -100,7 +207,7 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.rope_tab = rope_tab;
-  a.ws_acc = static_cast<float*>(workspace);
+  a.ws_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.acc_offset);
   a.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.ml_offset);
   a.status = dev_status;
   a.batch = batch;
@@ -120,9 +227,56 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
   a.vl = pool_layout(*cfg, 1);
 
   const int G = cfg->n_heads / cfg->n_kv_heads;
+  const int k = cfg->k_dtype, v = cfg->v_dtype;
+  if (w.tc) {
+    TcArgs t;
+    t.d = a;
+    t.out = out;
+    t.counters = static_cast<int32_t*>(workspace);
+    t.G = G;
+    t.blocks_per_chunk = w.blocks_per_chunk;
+    t.k_group_shift = __builtin_ctz((unsigned)cfg->k_group);
+    t.v_group_shift = __builtin_ctz((unsigned)cfg->v_group);
+    t.kc_bytes = cfg->page_size * a.kl.code_bytes;
+    t.vc_bytes = cfg->page_size * a.vl.code_bytes;
+    t.kp_bytes = cfg->page_size * a.kl.param_row_bytes;
+    t.vp_bytes = cfg->page_size * a.vl.param_row_bytes;
+    // Ring depth: pages in flight per warp group, as many as fit in about
+    // 60 KB of rings per CTA (three CTAs per SM), between 2 and kMaxDepth.
+    const int groups = cfg->head_dim == 256 ? 2 : 4;
+    const int page_all = t.kc_bytes + t.vc_bytes + t.kp_bytes + t.vp_bytes;
+    int depth = (60 * 1024) / (groups * page_all);
+    depth = depth < 2 ? 2 : (depth > kMaxDepth ? kMaxDepth : depth);
+    t.depth = depth;
+    t.ring_bytes = (depth * page_all + 1023) / 1024 * 1024;
+    size_t smem = (size_t)groups * t.ring_bytes;
+    const size_t ndim_states = 4 / (cfg->head_dim == 256 ? 2 : 1);
+    const size_t need_merge = (ndim_states * G * (cfg->head_dim + 2)) * sizeof(float);
+    const size_t need_comb = (size_t)w.n_chunks * G * 2 * sizeof(float);
+    if (smem < need_merge) smem = need_merge;
+    if (smem < need_comb) smem = need_comb;
+    smem += 1024;   // alignment of the swizzled boxes
+    if (smem > 200 * 1024)
+      return fail(KVQ_ERR_UNSUPPORTED, "decode needs %zu bytes of shared memory; use larger chunks", smem);
+    CUtensorMap mk, mv;
+    kvq_status st = code_map(&mk, k_pool, a.kl, n_pool_pages, cfg->n_kv_heads);
+    if (st == KVQ_OK) st = code_map(&mv, v_pool, a.vl, n_pool_pages, cfg->n_kv_heads);
+    if (st != KVQ_OK) return st;
+    const dim3 grid(w.tc_chunks, cfg->n_kv_heads, batch);
+    const bool pdl = pdl_enabled();
+    const int hdw = cfg->head_dim == 256 ? 128 : cfg->head_dim;   // dimensions per warp
+    const bool oneg = cfg->k_group >= hdw && cfg->v_group >= hdw;
+    const int hd = cfg->head_dim;
+    const int pt = cfg->k_param_dtype;
+    if (k == KVQ_SYM_INT4 && v == KVQ_SYM_INT4) st = launch_tc_s4s4(t, mk, mv, hd, oneg, pt, grid, smem, stream, pdl);
+    else if (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT8) st = launch_tc_s8s8(t, mk, mv, hd, oneg, pt, grid, smem, stream, pdl);
+    else if (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT4) st = launch_tc_s8s4(t, mk, mv, hd, oneg, pt, grid, smem, stream, pdl);
+    else st = launch_tc_a4a4(t, mk, mv, hd, oneg, pt, grid, smem, stream, pdl);
+    return st;
+  }
+
   const dim3 grid(w.n_chunks, cfg->n_kv_heads, batch);
   kvq_status st;
-  const int k = cfg->k_dtype, v = cfg->v_dtype;
   if (k == KVQ_SYM_INT4 && v == KVQ_SYM_INT4) st = launch_decode_s4s4(a, cfg->head_dim, G, grid, stream);
   else if (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT8) st = launch_decode_s8s8(a, cfg->head_dim, G, grid, stream);
   else if (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT4) st = launch_decode_s8s4(a, cfg->head_dim, G, grid, stream);
@@ -172,7 +326,7 @@ extern "C" size_t kvq_decode_workspace_bytes(const kvq_config* cfg, int32_t batc
     set_error("bad batch, max_pages_per_seq or chunk_tokens");
     return 0;
   }
-  return ws_layout(*cfg, batch, (int64_t)max_pages_per_seq * cfg->page_size, chunk_tokens).total;
+  return make_plan(*cfg, batch, (int64_t)max_pages_per_seq * cfg->page_size, false, chunk_tokens).total;
 }
 
 extern "C" size_t kvq_window_workspace_bytes(const kvq_config* cfg, int32_t batch, int32_t window,
@@ -183,7 +337,7 @@ extern "C" size_t kvq_window_workspace_bytes(const kvq_config* cfg, int32_t batc
     set_error("bad batch, window or chunk_tokens");
     return 0;
   }
-  return ws_layout(*cfg, batch, window, chunk_tokens).total;
+  return make_plan(*cfg, batch, window, true, chunk_tokens).total;
 }
 
 extern "C" kvq_status kvq_decode_attention(const kvq_config* cfg, int32_t batch, const void* q,

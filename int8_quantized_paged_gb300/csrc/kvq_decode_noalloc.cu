@@ -15,8 +15,9 @@
 // cudaGetSymbolAddress, on that device, the first time this entry point runs
 // there.  That first call should therefore come before any stream capture.
 // Every call shares the one array, so calls whose kernels overlap on the GPU
-// (for example on two streams at once) race on it.  The decode kernels write
-// every workspace entry they later read, so nothing has to be cleared between
+// (for example on two streams at once) race on it.  Its arrival counters
+// start at zero (static device memory is zero-initialised), and every
+// completed call leaves them zero again, so nothing has to be cleared between
 // calls.
 #include <cuda_runtime.h>
 

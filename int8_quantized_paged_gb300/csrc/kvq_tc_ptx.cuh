@@ -1,0 +1,218 @@
+// Inline-PTX helpers for the tensor-core decode kernel: TMA (tiled and bulk)
+// copies completed on mbarriers, bounded mbarrier waits, ldmatrix, mma.sync,
+// programmatic dependent launch, and exact code -> fp16 conversion.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace kvq {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `phase` of the barrier for at most `limit_ns`; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint64_t limit_ns = 1000000000ull) {
+  if (mbar_try_wait(bar, phase)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, phase)) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- TMA
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 3-D tiled copy of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Contiguous copy (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22, results
+// below 2^-126 flushed to zero); used for softmax weights in base 2.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------- PDL
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- ldmatrix / mma
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// D += A(16x16, row) * B(16x8, col); fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- codes -> fp16
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  __half2 x = *reinterpret_cast<__half2*>(&a);
+  __half2 y = *reinterpret_cast<__half2*>(&b);
+  __half2 r = __hsub2(x, y);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Codes of a packed word as exact half2 values, placed in the mantissa of
+// 1024 (0x6400) and the offset subtracted.  Symmetric 4-bit nibbles are XORed
+// with 8 (offset binary), affine nibbles are unsigned, and 8-bit codes are
+// XORed with 0x80.
+//
+// 4-bit, word x = nibbles n0..n7 (n_j at bits 4j):
+//   q4<0>(x) = (n0, n4)        q4<1>(x) = 16 * (n1, n5)
+//   q4<2>(x) = (n2, n6)        q4<3>(x) = 16 * (n3, n7)
+// The odd nibbles are taken where they lie (bits 4..7 of each half), which
+// gives 16 times the code, still exact in fp16.  The caller folds the 1/16
+// into the other operand or the result.  One shift (x >> 8) serves n2, n3,
+// n6 and n7.
+// 8-bit, word x = bytes b0..b3:  q8<0>(x) = (b0, b2),  q8<1>(x) = (b1, b3).
+template <bool AFF>
+__device__ __forceinline__ void q4_codes(uint32_t x, uint32_t (&h)[4]) {
+  const uint32_t y = x >> 8;
+  constexpr uint32_t X0 = AFF ? 0x64006400u : 0x64086408u;   // offset of n at bits 0..3
+  constexpr uint32_t X1 = AFF ? 0x64006400u : 0x64806480u;   // offset of n at bits 4..7
+  h[0] = hsub2_u32((x & 0x000F000Fu) ^ X0, X0);
+  h[1] = hsub2_u32((x & 0x00F000F0u) ^ X1, X1);
+  h[2] = hsub2_u32((y & 0x000F000Fu) ^ X0, X0);
+  h[3] = hsub2_u32((y & 0x00F000F0u) ^ X1, X1);
+}
+
+// The B operand pairs of P.V from two ldmatrix.trans words: b[s] = (q4<s>(xa),
+// q4<s>(xb)), produced pairwise so each pair can live in adjacent registers.
+template <bool AFF>
+__device__ __forceinline__ void q4_pairs(uint32_t xa, uint32_t xb, uint32_t (&b)[4][2]) {
+  const uint32_t ya = xa >> 8, yb = xb >> 8;
+  constexpr uint32_t X0 = AFF ? 0x64006400u : 0x64086408u;
+  constexpr uint32_t X1 = AFF ? 0x64006400u : 0x64806480u;
+  b[0][0] = hsub2_u32((xa & 0x000F000Fu) ^ X0, X0);
+  b[0][1] = hsub2_u32((xb & 0x000F000Fu) ^ X0, X0);
+  b[1][0] = hsub2_u32((xa & 0x00F000F0u) ^ X1, X1);
+  b[1][1] = hsub2_u32((xb & 0x00F000F0u) ^ X1, X1);
+  b[2][0] = hsub2_u32((ya & 0x000F000Fu) ^ X0, X0);
+  b[2][1] = hsub2_u32((yb & 0x000F000Fu) ^ X0, X0);
+  b[3][0] = hsub2_u32((ya & 0x00F000F0u) ^ X1, X1);
+  b[3][1] = hsub2_u32((yb & 0x00F000F0u) ^ X1, X1);
+}
+
+__device__ __forceinline__ void q8_codes(uint32_t x, uint32_t (&h)[2]) {
+  h[0] = hsub2_u32((x & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
+  h[1] = hsub2_u32(((x >> 8) & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// x = hi + lo * 2^-12 with both parts in fp16: hi = fp16(x) and
+// lo = fp16((x - hi) * 2^12).  The low part is stored 2^12 times larger so it
+// stays in fp16's normal range as long as hi does; its products are scaled
+// back by 2^-12 in fp32.
+constexpr float kLoScale = 4096.0f;
+__device__ __forceinline__ void split_half(float x, float& hi, float& lo) {
+  hi = __half2float(__float2half_rn(x));
+  lo = (x - hi) * kLoScale;
+}
+
+}  // namespace tc
+}  // namespace kvq

@@ -226,9 +226,11 @@ def test_device_calls_reject_bad_arguments_before_launch():
 def test_workspace_sizes():
     cfg = _host_cfg()
     a = kvq.decode_workspace_bytes(cfg, 4, 512, 256)
-    # 4 seqs x 8 kv heads x 32 chunks x 4 q heads x (128 acc + 2) floats, ml block 256-aligned
+    # counters (4 seqs x 8 kv heads, 256-aligned), then 32 chunks x 4 q heads x 128 fp32 partial
+    # sums per (seq, kv head), then (max, sum) pairs
+    counters = 256
     acc = 4 * 8 * 32 * 4 * 128 * 4
-    assert a == (acc + 255) // 256 * 256 + 4 * 8 * 32 * 4 * 2 * 4
+    assert a == counters + (acc + 255) // 256 * 256 + 4 * 8 * 32 * 4 * 2 * 4
     assert kvq.window_workspace_bytes(cfg, 1, 1024, 64) < kvq.decode_workspace_bytes(cfg, 1, 1024, 64)
     with pytest.raises(kvq.KvqError):
         kvq.decode_workspace_bytes(cfg, 1, 512, 20)
