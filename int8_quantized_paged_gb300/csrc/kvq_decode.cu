@@ -27,8 +27,8 @@ namespace kvq {
 static constexpr int kMaxChunks = 8192;
 
 // Whether the tensor-core kernel takes this config (and is not switched off):
-// power-of-two groups of at least 32 elements, code rows of 32..128 bytes, and
-// one stored type for the K and V scales.
+// power-of-two groups of at least 32 elements, a head_dim/G shape with an
+// instantiation, and one stored type for the K and V scales.
 static bool tc_enabled(const kvq_config& c) {
   static int forced = -1;
   if (forced < 0) {
@@ -36,10 +36,16 @@ static bool tc_enabled(const kvq_config& c) {
     forced = (e && std::strcmp(e, "simt") == 0) ? 0 : 1;
   }
   if (!forced) return false;
-  const int krb = c.k_dtype == KVQ_SYM_INT8 ? c.head_dim : c.head_dim / 2;
-  const int vrb = c.v_dtype == KVQ_SYM_INT8 ? c.head_dim : c.head_dim / 2;
   const bool pow2 = (c.k_group & (c.k_group - 1)) == 0 && (c.v_group & (c.v_group - 1)) == 0;
-  return pow2 && c.k_param_dtype == c.v_param_dtype && c.k_group >= 32 && c.v_group >= 32 && krb >= 32 && krb <= 128 && vrb >= 32 && vrb <= 128;
+  if (!pow2 || c.k_param_dtype != c.v_param_dtype || c.k_group < 32 || c.v_group < 32) return false;
+  const int G = c.n_heads / c.n_kv_heads;
+  return tc_has_shape(c.head_dim, G > 4 ? 2 : 1);
+}
+
+// CTAs of the tensor-core kernel resident per SM (its launch bounds).
+static int tc_resident(const kvq_config& c) {
+  const int G = c.n_heads / c.n_kv_heads;
+  return tc_min_blocks(c.head_dim, G > 4 ? 2 : 1);
 }
 
 static bool pdl_enabled() {
@@ -77,14 +83,15 @@ static Plan make_plan(const kvq_config& c, int32_t batch, int64_t max_tokens, bo
   if (requested > 0) {
     p.blocks_per_chunk = requested / P;
   } else {
-    const int64_t pairs = (int64_t)batch * c.n_kv_heads;
-    const int64_t slots = 2LL * num_sms();   // about one wave at two CTAs per SM
-    int64_t cb = (pairs * max_blocks + slots - 1) / slots;
-    const int spb = c.head_dim == 256 ? 2 : 4;   // pages per pipeline stage
-    cb = (cb + spb - 1) / spb * spb;
-    p.blocks_per_chunk = (int)(cb < 4 ? 4 : (cb > 64 ? 64 : cb));
+    // About whole waves of resident CTAs, assuming every sequence is as long
+    // as the longest, and at most 128 blocks per chunk.
+    const int64_t total = (int64_t)batch * c.n_kv_heads * max_blocks;
+    const int64_t wave = (int64_t)num_sms() * tc_resident(c);
+    const int64_t waves = (total + wave * 128 - 1) / (wave * 128);
+    int64_t cb = (total + waves * wave - 1) / (waves * wave);
+    cb = (cb + kWarps - 1) / kWarps * kWarps;
+    p.blocks_per_chunk = (int)(cb < 2 * kWarps ? 2 * kWarps : (cb > 128 ? 128 : cb));
   }
-  if (p.blocks_per_chunk > kMaxChunkBlocks) p.tc = false;
   const int64_t n_tc = (max_blocks + p.blocks_per_chunk - 1) / p.blocks_per_chunk;
   p.tc_chunks = (int)(n_tc < 1 ? 1 : (n_tc > (1 << 30) ? (1 << 30) : n_tc));
   const int64_t n = n_simt > n_tc ? n_simt : n_tc;
@@ -95,45 +102,6 @@ static Plan make_plan(const kvq_config& c, int32_t batch, int64_t max_tokens, bo
   p.ml_offset = p.acc_offset + (units * c.head_dim * sizeof(float) + 255) / 256 * 256;
   p.total = p.ml_offset + units * 2 * sizeof(float);
   return p;
-}
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// 3-D tensor map over the code rows of a pool: (row bytes, 16 rows, sub-block).
-static kvq_status code_map(CUtensorMap* map, const void* pool, const PoolLayout& L, int32_t n_pool_pages,
-                           int32_t n_kv_heads) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint32_t rowb = (cuuint32_t)L.code_bytes;
-  const cuuint64_t dims[3] = {rowb, 16, (cuuint64_t)n_pool_pages * n_kv_heads};
-  const cuuint64_t strides[2] = {rowb, (cuuint64_t)L.sub_bytes};
-  const cuuint32_t box[3] = {rowb, 16, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                : rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                             : CU_TENSOR_MAP_SWIZZLE_32B;
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  return KVQ_OK;
 }
 
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a, void* out, int G, int HD) {
@@ -241,37 +209,34 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     t.vc_bytes = cfg->page_size * a.vl.code_bytes;
     t.kp_bytes = cfg->page_size * a.kl.param_row_bytes;
     t.vp_bytes = cfg->page_size * a.vl.param_row_bytes;
-    // Ring depth: pages in flight per warp group, as many as fit in about
-    // 60 KB of rings per CTA (three CTAs per SM), between 2 and kMaxDepth.
-    const int groups = cfg->head_dim == 256 ? 2 : 4;
-    const int page_all = t.kc_bytes + t.vc_bytes + t.kp_bytes + t.vp_bytes;
-    int depth = (60 * 1024) / (groups * page_all);
-    depth = depth < 2 ? 2 : (depth > kMaxDepth ? kMaxDepth : depth);
-    t.depth = depth;
-    t.ring_bytes = (depth * page_all + 1023) / 1024 * 1024;
-    size_t smem = (size_t)groups * t.ring_bytes;
-    const size_t ndim_states = 4 / (cfg->head_dim == 256 ? 2 : 1);
-    const size_t need_merge = (ndim_states * G * (cfg->head_dim + 2)) * sizeof(float);
+    // Shared memory: a ring of tc_depth pages per warp, reused at the end for
+    // the warps' merge and the combine weights.
+    const int nt = G > 4 ? 2 : 1;
+    const bool oneg = cfg->k_group >= cfg->head_dim && cfg->v_group >= cfg->head_dim;
+    const int pt = cfg->k_param_dtype;
+    if (t.kp_bytes > tc_scale_bytes(k, cfg->head_dim, oneg, pt) || t.vp_bytes > tc_scale_bytes(v, cfg->head_dim, oneg, pt))
+      return fail(KVQ_ERR_UNSUPPORTED, "scale rows larger than the tensor-core kernel's slots");
+    size_t smem = (size_t)kWarps * tc_depth(cfg->head_dim, nt) * tc_slot_bytes(k, v, cfg->head_dim, oneg, pt);
+    const size_t need_merge = (size_t)kWarps * G * (cfg->head_dim + 2) * sizeof(float);
     const size_t need_comb = (size_t)w.n_chunks * G * 2 * sizeof(float);
     if (smem < need_merge) smem = need_merge;
     if (smem < need_comb) smem = need_comb;
-    smem += 1024;   // alignment of the swizzled boxes
     if (smem > 200 * 1024)
       return fail(KVQ_ERR_UNSUPPORTED, "decode needs %zu bytes of shared memory; use larger chunks", smem);
-    CUtensorMap mk, mv;
-    kvq_status st = code_map(&mk, k_pool, a.kl, n_pool_pages, cfg->n_kv_heads);
-    if (st == KVQ_OK) st = code_map(&mv, v_pool, a.vl, n_pool_pages, cfg->n_kv_heads);
-    if (st != KVQ_OK) return st;
+    kvq_status st = KVQ_OK;
     const dim3 grid(w.tc_chunks, cfg->n_kv_heads, batch);
     const bool pdl = pdl_enabled();
-    const int hdw = cfg->head_dim == 256 ? 128 : cfg->head_dim;   // dimensions per warp
-    const bool oneg = cfg->k_group >= hdw && cfg->v_group >= hdw;
     const int hd = cfg->head_dim;
-    const int pt = cfg->k_param_dtype;
-    if (k == KVQ_SYM_INT4 && v == KVQ_SYM_INT4) st = launch_tc_s4s4(t, mk, mv, hd, oneg, pt, grid, smem, stream, pdl);
-    else if (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT8) st = launch_tc_s8s8(t, mk, mv, hd, oneg, pt, grid, smem, stream, pdl);
-    else if (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT4) st = launch_tc_s8s4(t, mk, mv, hd, oneg, pt, grid, smem, stream, pdl);
-    else st = launch_tc_a4a4(t, mk, mv, hd, oneg, pt, grid, smem, stream, pdl);
+    static const TcLaunch table[4][3] = {
+        {launch_tc_s4s4_f32, launch_tc_s4s4_f16, launch_tc_s4s4_bf16},
+        {launch_tc_s8s8_f32, launch_tc_s8s8_f16, launch_tc_s8s8_bf16},
+        {launch_tc_s8s4_f32, launch_tc_s8s4_f16, launch_tc_s8s4_bf16},
+        {launch_tc_a4a4_f32, launch_tc_a4a4_f16, launch_tc_a4a4_bf16}};
+    const int kind = (k == KVQ_SYM_INT4 && v == KVQ_SYM_INT4) ? 0
+                     : (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT8) ? 1
+                     : (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT4) ? 2
+                                                                : 3;
+    st = table[kind][cfg->k_param_dtype](t, hd, nt, oneg, grid, smem, stream, pdl);
     return st;
   }
 

@@ -7,37 +7,42 @@
 // temporary tensor; §2.3: queries span fixed-size blocks; §3.4: fp32
 // softmax).
 //
-// Why tensor cores here: each code takes part in G multiply-adds for q.K
-// and G for p.V.  Done on the fp32 CUDA cores, that arithmetic plus the
-// dequantization issues more instructions per byte than the SMs can retire
-// at HBM speed.  So the codes go to mma.sync as exact fp16 integers, straight
-// from registers.  The packed nibbles are turned into fp16 fragments with a
-// mantissa trick and are never written back to shared memory.
+// Why tensor cores: every code takes part in G multiply-adds for q.K and G
+// for p.V.  On the fp32 CUDA cores that arithmetic, plus the dequantization,
+// needs more instructions per byte than the SMs retire at HBM speed.  So the
+// codes go to mma.sync as exact fp16 integers, converted in registers by a
+// mantissa trick and never written back to shared memory.
 //
-// Data movement: each warp (a warp pair for hd = 256) owns a ring of D page
-// slots in shared memory and takes every fourth (second) page of the chunk.
-// Its lane 0 issues the copies of a page and refills the slot as soon as the
-// warp is done with it, so D pages per warp stay in flight and no warp waits
-// for another.  Code rows use a 3-D TMA tiled copy with hardware swizzle, so
-// ldmatrix reads are free of bank conflicts.  Scales use a 1-D bulk copy.
-// Each slot completes on an mbarrier, and every wait has a time limit.
+// CTA = kWarps warps over one chunk of a (sequence, kv head).  Warp w takes
+// the chunk's pages w, w + kWarps, ... and keeps the next D of them in flight
+// in a private ring of page slots in shared memory: every lane issues 16-byte
+// cp.async copies of the page's K and V sub-blocks (codes and scales), one
+// commit group per page, so the warp waits only for its own oldest page.  The
+// code rows are written with an XOR swizzle of their 16-byte chunks, so the
+// ldmatrix reads below are free of bank conflicts.  A ring per warp, filled
+// by all of its lanes, keeps many independent copy streams per SM; a single
+// issuing thread per CTA refilling slots in page order does not saturate HBM
+// with 2 KB pages.
 //
-// Per warp and 16-token page (the G <= 8 query heads share one kv head):
-//   Q.K : S[16 x 16] = Qhl[16 x hd] * Khat^T.  Row g < G holds the fp16 high
-//         part of query head g (rotated, pre-scaled), row 8+g the low part
-//         (q = hi + lo * 2^-12), so the dot products keep about fp32 precision.
-//         Codes are exact in fp16.  Each scale group accumulates separately,
-//         and its scale (and affine bias * sum q) is applied in fp32 afterwards.
-//   softmax: online, base 2, in registers (4 scores per lane).  The running
-//         maximum is raised only when a page exceeds it by 2^8, so the
-//         accumulators are rescaled on few pages, and p <= 2^8.
-//   P.V : O[16 x hd] += W[16 x 16] * Vhat.  Rows g and 8+g hold hi and lo of
-//         w = p * scale * 2^7 / R (w = hi + lo * 2^-12), where R is the running
-//         maximum V scale of the group, so w stays inside fp16's range.
-// Warps own different pages and merge through shared memory at the end.
-// hd = 256 splits each page's dimensions over a pair of warps.  The pair
-// exchanges partial scores through shared memory under a 64-thread named
-// barrier.
+// Per warp and 16-token page (the G <= 8 query heads of one kv head):
+//   Q.K : S = Khat * Qhl, m16n8k16 with A = 16 tokens x 16 dims of codes and
+//         B = 16 dims x 8 columns.  Column 2h holds the fp16 high part of
+//         query head h (rotated, pre-scaled), column 2h+1 the low part
+//         (q = hi + lo * 2^-12), so the dot products keep about fp32
+//         precision.  A lane ends up with both parts of head h = lane % 4 for
+//         tokens lane/4 and lane/4 + 8.  Each scale group accumulates
+//         separately; its scale (and affine bias * sum q) applies in fp32.
+//   softmax: online, base 2.  The running maximum is raised only when a page
+//         exceeds it by 2^8, so the accumulators are rescaled on few pages,
+//         and p <= 2^8.
+//   P.V : O^T = Vhat^T * W, A = 16 dims x 16 tokens of codes (ldmatrix.trans),
+//         B = 16 tokens x 8 columns: column 2h the high part of
+//         w = p * scale * 2^7 / R, column 2h+1 the low part, where R is the
+//         running maximum V scale of the group (w stays inside fp16's range).
+//         w is formed where p lives and moved into the B layout with four
+//         shuffles.
+// Each warp keeps its own (m, l, O); the warps merge through shared memory at
+// the end.  G = 8 uses two 8-column tiles (NT = 2).
 #pragma once
 
 #include <cuda.h>
@@ -59,90 +64,106 @@ struct TcArgs {
   int32_t* counters;         // [batch][n_kv_heads] arrival tickets (zero between calls)
   int32_t G;                 // query heads per kv head (1..8)
   int32_t blocks_per_chunk;  // 16-token blocks per chunk
-  int32_t kc_bytes, vc_bytes, kp_bytes, vp_bytes;  // per page in shared memory
-  int32_t depth;                                   // ring slots (pages in flight) per warp group
-  int32_t ring_bytes;                              // shared memory of one group's ring
+  int32_t kc_bytes, vc_bytes, kp_bytes, vp_bytes;  // code and scale bytes of a page (one kv head)
   int32_t k_group_shift, v_group_shift;            // log2 of the group sizes
 };
 
-constexpr int kMaxDepth = 8;
-constexpr int kTcThreads = 128;
-constexpr int kMaxChunkBlocks = 256;
+constexpr int kWarps = 4;
+constexpr int kTcThreads = 32 * kWarps;
 constexpr float kQScale = 256.0f;   // q is held x 2^8 in fp16 (hi/lo)
 constexpr float kWScale = 128.0f;   // w is held x 2^7 (w <= 2^8 * 2^7 < 65504)
 constexpr float kLazyMax = 8.0f;    // raise the running max only past +2^8
 
-// Shared-memory offset of 16-byte chunk `c` of row `r` in a TMA box of rows of
-// ROWB bytes (32/64/128) written with the matching swizzle.
+// Pages in flight per warp, and CTAs per SM (the launch bounds), by shape.
+__host__ __device__ constexpr int tc_depth(int hd, int nt) { return hd == 256 ? 3 : (nt == 2 ? 4 : 6); }
+__host__ __device__ constexpr int tc_min_blocks(int hd, int nt) { return (hd <= 128 && nt == 1) ? 4 : 3; }
+
+// Shared-memory offset of 16-byte chunk `c` of row `r` in a block of rows of
+// ROWB bytes (32..256), with the chunk index XORed by a function of the row:
+// the eight rows an ldmatrix reads at one chunk land in eight different
+// 16-byte bank groups.
 template <int ROWB>
 __device__ __forceinline__ int swz(int r, int c) {
-  constexpr int SH = ROWB == 128 ? 0 : (ROWB == 64 ? 1 : 2);
-  constexpr int MASK = ROWB / 16 - 1;
-  return r * ROWB + ((c ^ ((r >> SH) & MASK)) << 4);
-}
-
-// Element of the head dimension held by lane (tig) in Q.K k-step `ks`,
-// fragment half f (0: k = 2tig, 2tig+1; 1: k = 2tig+8, 2tig+9), element e.
-template <int KK>
-__device__ __forceinline__ int qk_dim(int ks, int f, int e, int tig) {
-  if constexpr (KK == KVQ_SYM_INT8) {  // k-step = one 16-byte chunk = 16 elements
-    return 16 * ks + 4 * tig + f + 2 * e;
-  } else {  // two k-steps per 16-byte chunk of 32 nibbles
-    return 32 * (ks >> 1) + 8 * tig + 2 * (ks & 1) + f + 4 * e;
-  }
-}
-
-// Element of the head dimension of P.V n-tile j (0..3) of unit v, column n.
-template <int VK>
-__device__ __forceinline__ int pv_dim(int v, int j, int n) {
-  if constexpr (VK == KVQ_SYM_INT8) {
-    return 32 * v + 16 * (j >> 1) + 2 * n + (j & 1);
+  if constexpr (ROWB >= 128) {
+    return r * ROWB + ((c ^ (r & 7)) << 4);
   } else {
-    return 32 * v + 4 * n + j;
+    constexpr int SH = ROWB == 64 ? 1 : 2;
+    constexpr int MASK = ROWB / 16 - 1;
+    return r * ROWB + ((c ^ ((r >> SH) & MASK)) << 4);
   }
 }
 
-// A stored scale or bias of type PT (kvq_float) read from shared memory.
+// A stored scale or bias of type PT (kvq_float) at shared address `addr`.
 template <int PT>
-__device__ __forceinline__ float ld_param(const uint8_t* p) {
+__device__ __forceinline__ float ld_param(uint32_t addr) {
   if constexpr (PT == KVQ_F32) {
-    return *reinterpret_cast<const float*>(p);
-  } else if constexpr (PT == KVQ_F16) {
-    return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(p)));
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
   } else {
-    return __uint_as_float((uint32_t)(*reinterpret_cast<const unsigned short*>(p)) << 16);
+    unsigned short u;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(u) : "r"(addr) : "memory");
+    if constexpr (PT == KVQ_F16) return __half2float(__ushort_as_half(u));
+    return __uint_as_float((uint32_t)u << 16);
   }
 }
 
-// ONEG: one K scale group and one V scale group cover all of a warp's
-// dimensions, so each token has one K and one V scale per warp.
-// PT: the stored type of the scales (and biases) of both K and V.
-template <int KK, int VK, int HD, bool ONEG, int PT>
-__global__ void __launch_bounds__(kTcThreads, 3)
-decode_tc_kernel(const __grid_constant__ TcArgs A, const __grid_constant__ CUtensorMap tmap_k,
-                 const __grid_constant__ CUtensorMap tmap_v) {
+// Upper bound of the scale (and bias) bytes of one page of one kv head: one
+// group per head when ONEG, else groups of at least 32 elements.
+__host__ __device__ constexpr int tc_scale_bytes(int kind, int hd, bool oneg, int pt) {
+  return 16 * (oneg ? 1 : hd / 32) * (kind == KVQ_AFFINE_INT4 ? 2 : 1) * (pt == KVQ_F32 ? 4 : 2);
+}
+__host__ __device__ constexpr int tc_slot_bytes(int kk, int vk, int hd, bool oneg, int pt) {
+  return 16 * (kk == KVQ_SYM_INT8 ? hd : hd / 2) + 16 * (vk == KVQ_SYM_INT8 ? hd : hd / 2) +
+         tc_scale_bytes(kk, hd, oneg, pt) + tc_scale_bytes(vk, hd, oneg, pt);
+}
+
+// (hi, lo) fp16 parts of x packed as (low half, high half): x = hi + lo * 2^-12.
+__device__ __forceinline__ uint32_t hilo_pack(float x) {
+  const float hi = __half2float(__float2half_rn(x));
+  return tc::pack_half2(x, (x - hi) * tc::kLoScale);
+}
+
+// The high (part 0) or low (part 1) fp16 part of x, as a float.
+__device__ __forceinline__ float hilo_part(float x, int part) {
+  const float hi = __half2float(__float2half_rn(x));
+  return part ? (x - hi) * tc::kLoScale : x;
+}
+
+// KK / VK: code kinds of K and V.  HD: head dim.  NT: 8-column tiles (1 for
+// G <= 4, 2 for G = 8).  ONEG: one K group and one V group span the head.
+// PT: stored type of the scales (and biases) of K and V.
+template <int KK, int VK, int HD, int NT, bool ONEG, int PT>
+__global__ void __launch_bounds__(kTcThreads, tc_min_blocks(HD, NT))
+decode_tc_kernel(const __grid_constant__ TcArgs A) {
   constexpr int P = 16;
-  constexpr int DS = HD == 256 ? 2 : 1;          // warps per page (dimension split)
-  constexpr int HDW = HD / DS;                   // dimensions per warp
-  constexpr int NU = HDW / 32;                   // 32-element units per warp
-  constexpr int KRB = KK == KVQ_SYM_INT8 ? HD : HD / 2;   // K code row bytes
-  constexpr int VRB = VK == KVQ_SYM_INT8 ? HD : HD / 2;
-  constexpr int KCH = KRB / 16 / DS;             // K 16-byte chunks per warp
-  constexpr int VCH = VRB / 16 / DS;
-  constexpr int KS = KK == KVQ_SYM_INT8 ? KCH : 2 * KCH;  // Q.K k-steps per warp
-  constexpr int NSA = ONEG ? 1 : NU;             // score accumulators per n-tile
-  constexpr bool KAFF = KK == KVQ_AFFINE_INT4;
-  constexpr bool VAFF = VK == KVQ_AFFINE_INT4;
+  constexpr int NW = kWarps;
+  constexpr int D = tc_depth(HD, NT);           // pages in flight per warp
+  constexpr bool K8 = KK == KVQ_SYM_INT8, V8 = VK == KVQ_SYM_INT8;
+  constexpr bool KAFF = KK == KVQ_AFFINE_INT4, VAFF = VK == KVQ_AFFINE_INT4;
+  constexpr int KRB = K8 ? HD : HD / 2;          // K code row bytes
+  constexpr int VRB = V8 ? HD : HD / 2;
+  constexpr int KCH = KRB / 16;                  // 16-byte chunks per K row
+  constexpr int VCH = VRB / 16;
+  constexpr int KDC = K8 ? 16 : 32;              // dims per K chunk
+  constexpr int VDC = V8 ? 16 : 32;
+  constexpr int KSTEPS = K8 ? KCH : 2 * KCH;     // Q.K k-steps
+  constexpr int MT = HD / 16;                    // P.V m-tiles
+  constexpr int RUN = K8 ? 4 : 8;                // contiguous q dims a lane holds per K chunk
   constexpr int PB = PT == KVQ_F32 ? 4 : 2;      // bytes of a stored scale
-  static_assert(NU >= 2 && KCH % 2 == 0, "units");
+  constexpr int KNG = ONEG ? 1 : HD / 32;        // K groups held (upper bound when !ONEG)
+  constexpr int VNG = ONEG ? 1 : HD / 32;
+  // Ring slot: [K codes KC][V codes VC][K scales <= KPMAX][V scales <= VPMAX]
+  constexpr int KC = 16 * KRB, VC = 16 * VRB;
+  constexpr int KPMAX = tc_scale_bytes(KK, HD, ONEG, PT), VPMAX = tc_scale_bytes(VK, HD, ONEG, PT);
+  constexpr int SLOT = KC + VC + KPMAX + VPMAX;
+  // 16-byte copies per lane and page: lanes 0-15 copy the K sub-block, 16-31 the V one
+  constexpr int NCP = cmax((KC + KPMAX) / 16, (VC + VPMAX) / 16) / 16 + 1;
+  static_assert(KCH % 2 == 0 && VCH % 2 == 0, "chunk pairs");
 
   const DecodeArgs& a = A.d;
   const int G = A.G;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[4][kMaxDepth];   // a ring slot landed (TMA bytes)
-  __shared__ int32_t page_s[kMaxChunkBlocks];
-  __shared__ float q_s[8 * HD];                  // rotated, scaled queries
-  __shared__ float xs_s[2][2][P][8];             // hd = 256: partial scores of a warp pair
+  extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int32_t flag_s;
 
   const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -151,22 +172,6 @@ decode_tc_kernel(const __grid_constant__ TcArgs A, const __grid_constant__ CUten
 
   tc::grid_dependency_wait();   // inputs may come from the kernel before this one
 
-  // Page ids of the chunk's blocks (-1: not readable).  With the whole
-  // context attended, a chunk's blocks do not depend on the length, so the
-  // block-table entries are read together with seq_lens (one round trip).
-  const int32_t* bt = a.block_table + (int64_t)b * a.max_pages;
-  const int CB = A.blocks_per_chunk;
-  const int ring = a.ring_rows, npp = a.n_pool_pages;
-  const bool whole = a.window == 0 && ring == 0;
-  int pg_pre[2] = {-1, -1};
-  if (whole) {
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int j = tid + k * kTcThreads;
-      const int blk = chunk * CB + j;
-      if (j < CB && blk < a.max_pages) pg_pre[k] = bt[blk];
-    }
-  }
   const int L = a.seq_lens[b];
   int lo = 0, bad = 0;
   const int n_att = attended(a, L, &lo, &bad);
@@ -178,141 +183,154 @@ decode_tc_kernel(const __grid_constant__ TcArgs A, const __grid_constant__ CUten
     }
     return;
   }
+  const int CB = A.blocks_per_chunk;
   const int blk_lo = lo / P, blk_hi = (L + P - 1) / P;
   const int nch = (blk_hi - blk_lo + CB - 1) / CB;
   if (chunk >= nch) return;
   const int cb0 = blk_lo + chunk * CB;
   const int ncb = min(CB, blk_hi - cb0);
+  const int w = warp;
+  const int n_local = w < ncb ? (ncb - w + NW - 1) / NW : 0;   // pages w, w + NW, ... of the chunk
 
-  // 1024-aligned start of the dynamic region (TMA swizzle atoms), kept as an
-  // offset from the shared array so accesses stay in the shared space.
-  const int align = (1024 - (int)(tc::smem_u32(smem_raw) & 1023)) & 1023;
-  uint8_t* smem = smem_raw + align;
-  const uint32_t sbase = tc::smem_u32(smem);
-  const uint32_t bar0 = tc::smem_u32(&full_bar[0][0]);
-  if (tid == 0) {
-    for (int s = 0; s < 4 * kMaxDepth; ++s) tc::mbar_init(bar0 + 8 * s, 1);
-    tc::fence_barrier_init();
-    tc::prefetch_tensormap(&tmap_k);
-    tc::prefetch_tensormap(&tmap_v);
-  }
+  // ---- page ring of this warp: D slots of SLOT bytes.  Lane (hl = lane % 16)
+  // copies 16-byte chunks j = hl + 16 m of the page's K sub-block (lanes
+  // 0-15) or V sub-block (lanes 16-31): codes, then scales.
+  const uint32_t wring = tc::smem_u32(smem) + (uint32_t)(w * D * SLOT);
+  const bool vlane = lane >= 16;
+  const int hl = lane & 15;
+  const int n_sub = vlane ? (VC + A.vp_bytes) / 16 : (KC + A.kp_bytes) / 16;   // chunks of the sub-block
+  const int cnt = n_sub > hl ? (n_sub - hl + 15) / 16 : 0;                     // this lane's copies
+  uint32_t cp_dst[NCP];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int j = tid + k * kTcThreads;
-    if (j >= ncb) continue;
-    int pg;
-    if (whole) {
-      pg = pg_pre[k];
-    } else {
-      const int blk = cb0 + j;
-      const int row = ring > 0 ? (int)(((int64_t)blk * P) % ring) : blk * P;
-      pg = bt[row / P];
-    }
+  for (int m = 0; m < NCP; ++m) {
+    const int j = hl + 16 * m;
+    uint32_t d;
+    if (!vlane) d = j < KC / 16 ? swz<KRB>(j / KCH, j % KCH) : KC + VC + 16 * (j - KC / 16);
+    else d = j < VC / 16 ? KC + swz<VRB>(j / VCH, j % VCH) : KC + VC + KPMAX + 16 * (j - VC / 16);
+    cp_dst[m] = wring + d;
+  }
+  const int32_t* bt = a.block_table + (int64_t)b * a.max_pages;
+  const int ring = a.ring_rows, npp = a.n_pool_pages;
+  auto page_of = [&](int k) -> int {   // page id of this warp's k-th page, -1 if unreadable
+    const int blk = cb0 + w + NW * k;
+    const int idx = ring > 0 ? (int)(((int64_t)blk * P) % ring) / P : blk;
+    const int pg = bt[idx];
     const bool ok = pg >= 0 && pg < npp;
     if (!ok) report(a.status, KVQ_DEV_BAD_PAGE);
-    page_s[j] = ok ? pg : -1;
-  }
-  __syncthreads();
-
-  // ---- page rings: group g (a warp, or a warp pair for hd = 256) takes the
-  // chunk's pages g, g + NGRP, ...; its lane 0 keeps `depth` of them in flight.
-  constexpr int NGRP = 4 / DS;
-  const int depth = A.depth;
-  const int kc_bytes = A.kc_bytes, vc_bytes = A.vc_bytes, kp_bytes = A.kp_bytes, vp_bytes = A.vp_bytes;
-  const int grp = warp / DS;
-  const int n_local = grp < ncb ? (ncb - grp + NGRP - 1) / NGRP : 0;
-  const uint32_t rbase = sbase + grp * A.ring_bytes;       // [depth kc][depth vc][depth kp][depth vp]
-  const uint32_t gbar = bar0 + 8 * kMaxDepth * grp;
-  const bool producer = lane == 0 && (warp % DS) == 0;
-  const int64_t kpage = a.kl.page_bytes, vpage = a.vl.page_bytes;
-  const uint8_t* kbase = a.k_pool + (int64_t)kvh * a.kl.sub_bytes + P * a.kl.code_bytes;   // params of page 0
-  const uint8_t* vbase = a.v_pool + (int64_t)kvh * a.vl.sub_bytes + P * a.vl.code_bytes;
-  const int n_kv = a.n_kv_heads;
-  const uint32_t page_tx = (uint32_t)(kc_bytes + vc_bytes + kp_bytes + vp_bytes);
-
-  // Copy local page i of this group into slot i % depth.  The fence orders
-  // this group's earlier shared-memory reads of the slot before the copy.
-  auto issue = [&](int i) {
-    const int slot = i % depth;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    const uint32_t bar = gbar + 8 * slot;
-    const int pg = page_s[grp + i * NGRP];
-    if (pg < 0) {                       // unreadable page: complete the phase with no bytes
-      tc::mbar_arrive_expect_tx(bar, 0);
-      return;
-    }
-    tc::mbar_arrive_expect_tx(bar, page_tx);
-    const int z = pg * n_kv + kvh;
-    tc::tma_load_3d(rbase + slot * kc_bytes, &tmap_k, 0, 0, z, bar);
-    tc::tma_load_3d(rbase + depth * kc_bytes + slot * vc_bytes, &tmap_v, 0, 0, z, bar);
-    tc::bulk_load(rbase + depth * (kc_bytes + vc_bytes) + slot * kp_bytes, kbase + pg * kpage,
-                  (uint32_t)kp_bytes, bar);
-    tc::bulk_load(rbase + depth * (kc_bytes + vc_bytes + kp_bytes) + slot * vp_bytes, vbase + pg * vpage,
-                  (uint32_t)vp_bytes, bar);
+    return ok ? pg : -1;
   };
-  if (producer) {
-    for (int i = 0; i < min(n_local, depth); ++i) issue(i);
+  const uint8_t* pool_lane = (vlane ? a.v_pool + (int64_t)kvh * a.vl.sub_bytes
+                                    : a.k_pool + (int64_t)kvh * a.kl.sub_bytes) + 16 * hl;
+  const int64_t page_lane = vlane ? a.vl.page_bytes : a.kl.page_bytes;
+  int ids = n_local > 0 ? page_of(min(lane, n_local - 1)) : -1;   // page ids of pages 32q .. 32q+31
+  uint32_t valid = 0;                                               // bit s: slot s holds a page
+  auto issue = [&](int k, int s) {   // all lanes: copies of page k into slot s
+    if ((k & 31) == 0 && k > 0) ids = page_of(min(k + lane, n_local - 1));
+    const int pg = __shfl_sync(0xffffffffu, ids, k & 31);
+    valid = pg >= 0 ? (valid | (1u << s)) : (valid & ~(1u << s));
+    if (pg < 0) return;
+    const uint8_t* src = pool_lane + pg * page_lane;
+#pragma unroll
+    for (int m = 0; m < NCP; ++m)
+      if (m < cnt)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(cp_dst[m] + s * SLOT), "l"(src + 256 * m)
+                     : "memory");
+  };
+#pragma unroll
+  for (int k = 0; k < D; ++k) {
+    if (k < n_local) issue(k, k);
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
 
-  // rotated queries at position L-1, scaled by alpha * log2(e) * 2^8 (while
-  // the first stages are in flight)
+  // ---- query fragments.  Lane (gid, tig) holds, for column gid (head
+  // hq = gid / 2, part gid % 2), the q elements its K k-steps meet: the runs
+  // of RUN dims starting at KDC*c + RUN*tig of every K chunk c.
+  uint32_t qb[NT][KSTEPS][2];
+  float qsum[NT][KNG];   // affine K: sum of q over each group for the score head
   {
+    const int part = gid & 1;
     const float2* cs = reinterpret_cast<const float2*>(a.rope_tab) + (int64_t)(L - 1) * (HD / 2);
     const float sc = a.score_scale * kQScale;
     const int rope = a.rope, act = a.act;
-    const bool neox = rope == KVQ_ROPE_NEOX;
-    for (int i = tid; i < G * (HD / 2); i += kTcThreads) {
-      const int h = i / (HD / 2), pi = i - h * (HD / 2);
-      const int d0 = neox ? pi : 2 * pi;
-      const int d1 = neox ? pi + HD / 2 : 2 * pi + 1;
-      float x0 = load_act(a.q, act, obase + h * HD + d0);
-      float x1 = load_act(a.q, act, obase + h * HD + d1);
-      if (rope != KVQ_ROPE_NONE) {
-        const float2 t = cs[pi];
-        const float r0 = x0 * t.x - x1 * t.y;
-        const float r1 = x0 * t.y + x1 * t.x;
-        x0 = r0;
-        x1 = r1;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int hq = NT == 1 ? (gid >> 1) % G : 4 * nt + (gid >> 1);
+      const int64_t qoff = obase + (int64_t)hq * HD;
+      float qv[KCH][RUN];
+#pragma unroll
+      for (int c = 0; c < KCH; ++c)
+#pragma unroll
+        for (int k = 0; k < RUN; ++k) qv[c][k] = load_act(a.q, act, qoff + KDC * c + RUN * tig + k);
+      if (rope == KVQ_ROPE_NORMAL) {   // pairs (2i, 2i+1) lie inside a run
+#pragma unroll
+        for (int c = 0; c < KCH; ++c)
+#pragma unroll
+          for (int k = 0; k < RUN; k += 2) {
+            const float2 t = cs[(KDC * c + RUN * tig + k) >> 1];
+            const float x0 = qv[c][k], x1 = qv[c][k + 1];
+            qv[c][k] = x0 * t.x - x1 * t.y;
+            qv[c][k + 1] = x0 * t.y + x1 * t.x;
+          }
+      } else if (rope == KVQ_ROPE_NEOX) {   // pairs (i, i + HD/2): chunk c with chunk c + KCH/2
+#pragma unroll
+        for (int c = 0; c < KCH / 2; ++c)
+#pragma unroll
+          for (int k = 0; k < RUN; ++k) {
+            const float2 t = cs[KDC * c + RUN * tig + k];
+            const float x0 = qv[c][k], x1 = qv[c + KCH / 2][k];
+            qv[c][k] = x0 * t.x - x1 * t.y;
+            qv[c + KCH / 2][k] = x0 * t.y + x1 * t.x;
+          }
       }
-      q_s[h * HD + d0] = x0 * sc;
-      q_s[h * HD + d1] = x1 * sc;
-    }
-  }
-  __syncthreads();
-
-  // ---- this lane's query fragments (fp16 hi/lo) and per-unit query sums.
-  // 4-bit K: the codes in fragment half f = 1 come as 16 * code, so the
-  // query elements they meet are divided by 16 here.
-  const int half = DS == 2 ? (warp & 1) : 0;     // which half of the dims this warp owns
-  const int dim0 = half * HDW;
-  const bool live = gid < G;
-  uint32_t qa[KS][4];
-  float qsum[NU];
 #pragma unroll
-  for (int u = 0; u < NU; ++u) qsum[u] = 0.f;
+      for (int c = 0; c < KCH; ++c)
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    float hv[2][2], lv[2][2];
+        for (int k = 0; k < RUN; ++k) qv[c][k] *= sc;
+      // B fragments: 4-bit K chunk c, parity p (p = 1 meets 16 * code, so q / 16):
+      //   b0 = q at dims KDC*c + 8tig + p + {0, 4},  b1 = dims + {2, 6}
+      // 8-bit K chunk c:  b0 = dims 16c + 4tig + {0, 2},  b1 = dims + {1, 3}
 #pragma unroll
-    for (int f = 0; f < 2; ++f)
+      for (int c = 0; c < KCH; ++c) {
+        if constexpr (K8) {
+          qb[nt][c][0] = tc::pack_half2(hilo_part(qv[c][0], part), hilo_part(qv[c][2], part));
+          qb[nt][c][1] = tc::pack_half2(hilo_part(qv[c][1], part), hilo_part(qv[c][3], part));
+        } else {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float x = live ? q_s[gid * HD + dim0 + qk_dim<KK>(ks, f, e, tig)] : 0.f;
-        qsum[ks >> 1] += x;
-        const float xs = (KK != KVQ_SYM_INT8 && f == 1) ? x * (1.0f / 16.0f) : x;
-        tc::split_half(xs, hv[f][e], lv[f][e]);
+          for (int p = 0; p < 2; ++p) {
+            const float f = p ? 1.0f / 16.0f : 1.0f;
+            qb[nt][2 * c + p][0] =
+                tc::pack_half2(hilo_part(qv[c][p] * f, part), hilo_part(qv[c][p + 4] * f, part));
+            qb[nt][2 * c + p][1] =
+                tc::pack_half2(hilo_part(qv[c][p + 2] * f, part), hilo_part(qv[c][p + 6] * f, part));
+          }
+        }
       }
-    qa[ks][0] = tc::pack_half2(hv[0][0], hv[0][1]);   // row gid     : hi, k = 2tig, 2tig+1
-    qa[ks][1] = tc::pack_half2(lv[0][0], lv[0][1]);   // row gid + 8 : lo
-    qa[ks][2] = tc::pack_half2(hv[1][0], hv[1][1]);   // row gid     : hi, k = 2tig+8, 2tig+9
-    qa[ks][3] = tc::pack_half2(lv[1][0], lv[1][1]);   // row gid + 8 : lo
-  }
-  if constexpr (KAFF) {
+      // affine K: per-group q sums, gathered for the lane's score head 4nt + tig
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {
-      qsum[u] += __shfl_xor_sync(0xffffffffu, qsum[u], 1);
-      qsum[u] += __shfl_xor_sync(0xffffffffu, qsum[u], 2);
-      qsum[u] *= 1.0f / kQScale;
+      for (int g = 0; g < KNG; ++g) qsum[nt][g] = 0.f;
+      if constexpr (KAFF) {
+        float part_sum[KNG];
+#pragma unroll
+        for (int g = 0; g < KNG; ++g) part_sum[g] = 0.f;
+#pragma unroll
+        for (int c = 0; c < KCH; ++c) {
+          const int g = ONEG ? 0 : ((KDC * c) >> A.k_group_shift);
+#pragma unroll
+          for (int gg = 0; gg < KNG; ++gg)
+            if (gg == g)
+#pragma unroll
+              for (int k = 0; k < RUN; ++k) part_sum[gg] += qv[c][k];
+        }
+#pragma unroll
+        for (int g = 0; g < KNG; ++g) {
+          float v = part_sum[g];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          // lane 8h holds head h (gid = 2h, part hi) of this tile
+          const int hs = NT == 1 ? tig % G : tig;
+          qsum[nt][g] = __shfl_sync(0xffffffffu, v, 8 * hs) * (1.0f / kQScale);
+        }
+      }
     }
   }
 
@@ -321,300 +339,340 @@ decode_tc_kernel(const __grid_constant__ TcArgs A, const __grid_constant__ CUten
   const int kstep = a.kl.n_params * PB, vstep = a.vl.n_params * PB;   // bytes per group in a param row
   const int mi = lane >> 3;
   const int trow = 8 * (mi & 1) + (lane & 7);    // token row this lane addresses in ldmatrix
-  const int tok0 = 2 * tig;                      // the lane's tokens: tok0, tok0+1, tok0+8, tok0+9
-  int gk[NU], gv[NU];                            // scale-group index of each unit
+  int kls[KCH / 2], vls[VCH / 2];
 #pragma unroll
-  for (int u = 0; u < NU; ++u) {
-    gk[u] = (dim0 + 32 * u) >> A.k_group_shift;
-    gv[u] = (dim0 + 32 * u) >> A.v_group_shift;
-  }
-  int kpo[4], vpo[4];                            // param-row offsets of the lane's tokens
+  for (int c = 0; c < KCH; c += 2) kls[c / 2] = swz<KRB>(trow, c + (mi >> 1));
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = tok0 + (i & 1) + 8 * (i >> 1);
-    kpo[i] = t * kprb + (ONEG ? gk[0] * kstep : 0);
-    vpo[i] = t * vprb + (ONEG ? gv[0] * vstep : 0);
-  }
-  const int pair = warp >> 1;
-  // ldmatrix lane offsets within a page's code rows (chunk pair c, c+1)
-  int kls[KCH / 2], vls[(VK == KVQ_SYM_INT8 ? VCH : VCH) / 2];
-#pragma unroll
-  for (int c = 0; c < KCH; c += 2) kls[c / 2] = swz<KRB>(trow, half * KCH + c + (mi >> 1));
-#pragma unroll
-  for (int c = 0; c < VCH; c += 2) vls[c / 2] = swz<VRB>(trow, half * VCH + c + (mi >> 1));
-  // ---- per-warp running state
-  float m = -INFINITY, l = 0.f;
-  float oacc[NU][4][4];
-  float pb[NU];       // affine V: sum of p * bias per unit
-  float vref[NU];     // reference V scale of each unit's group (w = p * scale * 2^7 / vref)
-  float vinv[NU];     // 2^7 / vref (0 before the first page)
-#pragma unroll
-  for (int u = 0; u < NU; ++u) {
-    pb[u] = 0.f;
-    vref[u] = 0.f;
-    vinv[u] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) oacc[u][j][e] = 0.f;
-  }
-  bool timed_out = false;
+  for (int c = 0; c < VCH; c += 2) vls[c / 2] = swz<VRB>(trow, c + (mi >> 1));
+  // P.V transposition: the B column of this lane is head hq (part gid % 2);
+  // its tokens 2tig, 2tig+1 (+8) come from lanes src0, src1.
+  const int src_tig = NT == 1 ? (gid >> 1) % G : (gid >> 1);
+  const int src0 = 8 * tig + src_tig, src1 = src0 + 4;
+  const uint32_t psel = (gid & 1) ? 0x7632u : 0x5410u;
 
-  for (int i = 0; i < n_local; ++i) {
-    const int slot = i % depth;
-    if (!tc::mbar_wait(gbar + 8 * slot, (uint32_t)((i / depth) & 1))) timed_out = true;
-    const int blk = grp + i * NGRP;
-    {
-      const bool have = page_s[blk] >= 0;
-      const uint32_t kc = rbase + slot * kc_bytes;
-      const uint32_t vc = rbase + depth * kc_bytes + slot * vc_bytes;
-      const uint8_t* kp = smem + grp * A.ring_bytes + depth * (kc_bytes + vc_bytes) + slot * kp_bytes;
-      const uint8_t* vp = smem + grp * A.ring_bytes + depth * (kc_bytes + vc_bytes + kp_bytes) + slot * vp_bytes;
-      const int tb = (cb0 + blk) * P;           // absolute token index of the page's slot 0
+  // ---- running state: head 4nt + tig (mod G) of this lane
+  float m[NT], l[NT];
+  float oacc[MT][NT][4];
+  float pbias[NT][VNG];   // affine V: sum of p * bias per group
+  float vinv[VNG];        // 2^7 / R, R the reference V scale of the group (0: none yet)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt] = -INFINITY;
+    l[nt] = 0.f;
+#pragma unroll
+    for (int g = 0; g < VNG; ++g) pbias[nt][g] = 0.f;
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oacc[t][nt][e] = 0.f;
+  }
+#pragma unroll
+  for (int g = 0; g < VNG; ++g) vinv[g] = 0.f;
 
-      float s[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (have) {
-        // ---- Q.K on tensor cores
-        float sacc[NSA][2][4];
+  int s = 0;   // slot of page k: k % D
+#pragma unroll 1
+  for (int k = 0; k < n_local; ++k) {
+    const int i = w + k * NW;   // block of the chunk
+    // page k landed: at most D - 1 younger commit groups of this lane pending,
+    // and the warp's lanes see each other's copies after the sync
+    asm volatile("cp.async.wait_group %0;" ::"n"(D - 1) : "memory");
+    __syncwarp();
+    if ((valid >> s) & 1u) {
+      const uint32_t kc = wring + s * SLOT;
+      const uint32_t vc = kc + KC;
+      const uint32_t kp = kc + KC + VC;
+      const uint32_t vp = kp + KPMAX;
+      const int tb = (cb0 + i) * P;   // absolute token index of the page's row 0
+      const bool edge = tb < lo || tb + P > L;
+
+      // ---- Q.K: A = codes of tokens (gid, gid+8), B = q fragments
+      float s[NT][2];
 #pragma unroll
-        for (int u = 0; u < NSA; ++u)
+      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = 0.f;
+      float sacc[NT][4];
 #pragma unroll
-          for (int n = 0; n < 2; ++n)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[u][n][e] = 0.f;
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+      // fold the accumulated dots of K group g into the scores
+      auto fold = [&](int g) {
 #pragma unroll
-        for (int c = 0; c < KCH; c += 2) {
-          uint32_t r[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
-          tc::ldsm_x4(kc + kls[c / 2], r);
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t pr = kp + (gid + 8 * j) * kprb + g * kstep;
+          const float ks = ld_param<PT>(pr) * (1.0f / kQScale);
+          float kb = 0.f;
+          if constexpr (KAFF) kb = ld_param<PT>(pr + PB);
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int ch = c + cc;
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-              if constexpr (KK == KVQ_SYM_INT8) {
-                uint32_t h[2];
-                tc::q8_codes(r[2 * cc + n], h);
-                tc::mma_16816(sacc[ONEG ? 0 : (ch >> 1)][n], qa[ch], h[0], h[1]);
-              } else {
-                uint32_t h[4];
-                tc::q4_codes<KAFF>(r[2 * cc + n], h);
-                tc::mma_16816(sacc[ONEG ? 0 : ch][n], qa[2 * ch], h[0], h[1]);
-                tc::mma_16816(sacc[ONEG ? 0 : ch][n], qa[2 * ch + 1], h[2], h[3]);
-              }
-            }
-          }
-        }
-        // ---- scores of the lane's 4 tokens for head gid
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int n = i >> 1, e = i & 1;
-          if constexpr (ONEG) {
-            const float ks = ld_param<PT>(kp + kpo[i]) * (1.0f / kQScale);
-            float v = ks * fmaf(sacc[0][n][e + 2], 1.0f / tc::kLoScale, sacc[0][n][e]);
+          for (int nt = 0; nt < NT; ++nt) {
+            float v = ks * fmaf(sacc[nt][2 * j + 1], 1.0f / tc::kLoScale, sacc[nt][2 * j]);
             if constexpr (KAFF) {
-              float qs = 0.f;
+              float qs = qsum[nt][0];
 #pragma unroll
-              for (int u = 0; u < NU; ++u) qs += qsum[u];
-              v = fmaf(ld_param<PT>(kp + kpo[i] + PB), qs, v);
+              for (int gg = 1; gg < KNG; ++gg)
+                if (gg == g) qs = qsum[nt][gg];
+              v = fmaf(kb, qs, v);
             }
-            s[i] = v;
+            s[nt][j] += v;
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+      };
+#pragma unroll
+      for (int c2 = 0; c2 < KCH / 2; ++c2) {
+        uint32_t r[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
+        tc::ldsm_x4(kc + kls[c2], r);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * c2 + cc;
+          if constexpr (K8) {
+            uint32_t h0[2], h8[2];
+            tc::q8_codes(r[2 * cc], h0);
+            tc::q8_codes(r[2 * cc + 1], h8);
+            const uint32_t af[4] = {h0[0], h8[0], h0[1], h8[1]};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) tc::mma_16816(sacc[nt], af, qb[nt][c][0], qb[nt][c][1]);
           } else {
-            float acc = 0.f, part = 0.f, qs = 0.f;
+            uint32_t h0[4], h8[4];
+            tc::q4_codes<KAFF>(r[2 * cc], h0);
+            tc::q4_codes<KAFF>(r[2 * cc + 1], h8);
+            const uint32_t ae[4] = {h0[0], h8[0], h0[2], h8[2]};
+            const uint32_t ao[4] = {h0[1], h8[1], h0[3], h8[3]};
 #pragma unroll
-            for (int u = 0; u < NU; ++u) {
-              part += fmaf(sacc[u][n][e + 2], 1.0f / tc::kLoScale, sacc[u][n][e]);
-              if constexpr (KAFF) qs += qsum[u];
-              if (u == NU - 1 || gk[u + 1] != gk[u]) {   // end of a group's units
-                const uint8_t* pg = kp + kpo[i] + gk[u] * kstep;
-                acc = fmaf(ld_param<PT>(pg) * (1.0f / kQScale), part, acc);
-                if constexpr (KAFF) acc = fmaf(ld_param<PT>(pg + PB), qs, acc);
-                part = 0.f;
-                qs = 0.f;
-              }
+            for (int nt = 0; nt < NT; ++nt) {
+              tc::mma_16816(sacc[nt], ae, qb[nt][2 * c][0], qb[nt][2 * c][1]);
+              tc::mma_16816(sacc[nt], ao, qb[nt][2 * c + 1][0], qb[nt][2 * c + 1][1]);
             }
-            s[i] = acc;
+          }
+          if constexpr (!ONEG) {
+            if (((KDC * (c + 1)) & ((1 << A.k_group_shift) - 1)) == 0) fold((KDC * c) >> A.k_group_shift);
           }
         }
       }
-      if constexpr (DS == 2) {   // add the partner warp's half of each dot product
+      if constexpr (ONEG) fold(0);
+      if (edge) {   // the page at the window start or the context end
 #pragma unroll
-        for (int i = 0; i < 4; ++i) xs_s[pair][half][tok0 + (i & 1) + 8 * (i >> 1)][gid] = s[i];
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
+        for (int j = 0; j < 2; ++j) {
+          const int t = tb + gid + 8 * j;
+          if (t < lo || t >= L)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s[i] += xs_s[pair][half ^ 1][tok0 + (i & 1) + 8 * (i >> 1)][gid];
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
-      }
-      if (tb < lo || tb + P > L) {   // a page at the window start or the context end
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int t = tb + tok0 + (i & 1) + 8 * (i >> 1);
-          if (t < lo || t >= L) s[i] = -INFINITY;
+            for (int nt = 0; nt < NT; ++nt) s[nt][j] = -INFINITY;
         }
       }
+
       // ---- online softmax (base 2), running max raised lazily
-      float bm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-      if (bm > m + kLazyMax) {
-        if (m != -INFINITY) {
-          const float corr = tc::ex2(m - bm);
-          l *= corr;
+      bool raise = false;
 #pragma unroll
-          for (int u = 0; u < NU; ++u) {
-            pb[u] *= corr;
+      for (int nt = 0; nt < NT; ++nt) raise |= fmaxf(s[nt][0], s[nt][1]) > m[nt] + kLazyMax;
+      if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+        for (int nt = 0; nt < NT; ++nt) {
+          float bm = fmaxf(s[nt][0], s[nt][1]);
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+          if (bm > m[nt] + kLazyMax) {
+            const float corr = m[nt] == -INFINITY ? 0.f : tc::ex2(m[nt] - bm);
+            l[nt] *= corr;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) oacc[u][j][e] *= corr;
+            for (int g = 0; g < VNG; ++g) pbias[nt][g] *= corr;
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) oacc[t][nt][e] *= corr;
+            m[nt] = bm;
           }
         }
-        m = bm;
       }
-      float p[4];
+      float p[NT][2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) p[i] = tc::ex2(s[i] - m);   // 0 for masked tokens (s = -inf)
-      if (m == -INFINITY) p[0] = p[1] = p[2] = p[3] = 0.f;
-      float ps = (p[0] + p[1]) + (p[2] + p[3]);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-      l += ps;
-      // ---- P.V on tensor cores (one weight fragment per V group)
-      if (have && __any_sync(0xffffffffu, ps > 0.f)) {
-        uint32_t wa[4] = {0u, 0u, 0u, 0u};
-        uint32_t r[4] = {0u, 0u, 0u, 0u};
+      for (int nt = 0; nt < NT; ++nt) {
+        const float mu = m[nt] == -INFINITY ? 0.f : m[nt];
+        p[nt][0] = tc::ex2(s[nt][0] - mu);   // 0 for masked tokens (s = -inf)
+        p[nt][1] = tc::ex2(s[nt][1] - mu);
+        l[nt] += p[nt][0] + p[nt][1];
+      }
+
+      // ---- P.V: A = V^T codes (ldmatrix.trans), B = weights of V group g.
+      // Entering group g: its scales for the lane's tokens (gid, gid+8), a
+      // raise of its reference when a scale passes half of it (2x headroom),
+      // then w = p * scale * vinv formed here and moved to the B layout.
+      uint32_t bw[NT][2];
+      auto weights = [&](int g) {
+        float vs[2], vb[2] = {0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < NU; ++u) {
-          if (u == 0 || (!ONEG && gv[u] != gv[u - 1])) {   // weights of this V group
-            float sc[4], vb4[4];
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t pr = vp + (gid + 8 * j) * vprb + g * vstep;
+          vs[j] = ld_param<PT>(pr);
+          if constexpr (VAFF) vb[j] = ld_param<PT>(pr + PB);
+          if (edge) {
+            const int t = tb + gid + 8 * j;
+            if (t < lo || t >= L) vs[j] = vb[j] = 0.f;
+          }
+        }
+        float vig = vinv[0];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint8_t* pg = vp + vpo[i] + (ONEG ? 0 : gv[u] * vstep);
-              sc[i] = ld_param<PT>(pg);
-              vb4[i] = VAFF ? ld_param<PT>(pg + PB) : 0.f;
-            }
-            float smax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
-            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
-            if (smax > vref[u]) {   // raise the group's reference (2x headroom), rescale its sums
-              const float nref = 2.0f * smax;
-              if (vref[u] > 0.f) {
-                const float ratio = vref[u] / nref;
+        for (int gg = 1; gg < VNG; ++gg)
+          if (gg == g) vig = vinv[gg];
+        // a scale above half the reference: 2 * scale * vinv > kWScale
+        if (__any_sync(0xffffffffu, 2.0f * fmaxf(vs[0], vs[1]) * vig > kWScale || vig == 0.f)) {
+          float sm = fmaxf(vs[0], vs[1]);
+          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 4));
+          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 8));
+          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 16));
+          if (sm > 0.f && (vig == 0.f || 2.0f * sm * vig > kWScale)) {
+            const float nvi = kWScale / (2.0f * sm);
+            if (vig > 0.f) {
+              const float ratio = nvi / vig;
 #pragma unroll
-                for (int uu = 0; uu < NU; ++uu) {
-                  if (gv[uu] != gv[u]) continue;
+              for (int t = 0; t < MT; ++t) {
+                const int c = V8 ? t : (t >> 1);
+                if (ONEG || ((VDC * c) >> A.v_group_shift) == g)
 #pragma unroll
-                  for (int j = 0; j < 4; ++j)
+                  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) oacc[uu][j][e] *= ratio;
-                }
+                    for (int e = 0; e < 4; ++e) oacc[t][nt][e] *= ratio;
               }
-              const float ninv = kWScale / nref;
-#pragma unroll
-              for (int uu = 0; uu < NU; ++uu)
-                if (gv[uu] == gv[u]) {
-                  vref[uu] = nref;
-                  vinv[uu] = ninv;
-                }
             }
-            const float inv = vinv[u];
-            float wh[4], wl[4];
+            vig = nvi;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tc::split_half(p[i] * (sc[i] * inv), wh[i], wl[i]);
-            wa[0] = tc::pack_half2(wh[0], wh[1]);   // row gid     : hi, tokens tok0, tok0+1
-            wa[1] = tc::pack_half2(wl[0], wl[1]);   // row gid + 8 : lo
-            wa[2] = tc::pack_half2(wh[2], wh[3]);   // row gid     : hi, tokens tok0+8, tok0+9
-            wa[3] = tc::pack_half2(wl[2], wl[3]);   // row gid + 8 : lo
-            if constexpr (VAFF) {
-              const float add = (p[0] * vb4[0] + p[1] * vb4[1]) + (p[2] * vb4[2] + p[3] * vb4[3]);
-#pragma unroll
-              for (int uu = 0; uu < NU; ++uu)
-                if (gv[uu] == gv[u]) pb[uu] += add;
-            }
+            for (int gg = 0; gg < VNG; ++gg)
+              if (gg == g) vinv[gg] = nvi;
           }
-          if constexpr (VK == KVQ_SYM_INT8) {   // unit = two 16-byte chunks
-            tc::ldsm_x4_trans(vc + vls[u], r);
+        }
+        if constexpr (VAFF) {
 #pragma unroll
-            for (int kap = 0; kap < 2; ++kap) {
-              uint32_t ha[2], hb[2];
-              tc::q8_codes(r[2 * kap], ha);
-              tc::q8_codes(r[2 * kap + 1], hb);
-              tc::mma_16816(oacc[u][2 * kap], wa, ha[0], hb[0]);
-              tc::mma_16816(oacc[u][2 * kap + 1], wa, ha[1], hb[1]);
+          for (int gg = 0; gg < VNG; ++gg)
+            if (gg == g)
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                pbias[nt][gg] = fmaf(p[nt][0], vb[0], fmaf(p[nt][1], vb[1], pbias[nt][gg]));
+        }
+        const float w0 = vs[0] * vig, w1 = vs[1] * vig;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t r0 = hilo_pack(p[nt][0] * w0);   // token gid
+          const uint32_t r1 = hilo_pack(p[nt][1] * w1);   // token gid + 8
+          const uint32_t u00 = __shfl_sync(0xffffffffu, r0, src0);  // token 2tig
+          const uint32_t u10 = __shfl_sync(0xffffffffu, r0, src1);  // token 2tig + 1
+          const uint32_t u01 = __shfl_sync(0xffffffffu, r1, src0);  // token 2tig + 8
+          const uint32_t u11 = __shfl_sync(0xffffffffu, r1, src1);  // token 2tig + 9
+          bw[nt][0] = __byte_perm(u00, u10, psel);
+          bw[nt][1] = __byte_perm(u01, u11, psel);
+        }
+      };
+      if constexpr (ONEG) weights(0);
+#pragma unroll
+      for (int c2 = 0; c2 < VCH / 2; ++c2) {
+        uint32_t y[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
+        tc::ldsm_x4_trans(vc + vls[c2], y);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * c2 + cc;
+          if constexpr (!ONEG) {
+            if (((VDC * c) & ((1 << A.v_group_shift) - 1)) == 0) weights((VDC * c) >> A.v_group_shift);
+          }
+          if constexpr (V8) {
+            uint32_t h0[2], h8[2];
+            tc::q8_codes(y[2 * cc], h0);
+            tc::q8_codes(y[2 * cc + 1], h8);
+            const uint32_t af[4] = {h0[0], h0[1], h8[0], h8[1]};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) tc::mma_16816(oacc[c][nt], af, bw[nt][0], bw[nt][1]);
+          } else {
+            uint32_t h0[4], h8[4];
+            tc::q4_codes<VAFF>(y[2 * cc], h0);
+            tc::q4_codes<VAFF>(y[2 * cc + 1], h8);
+#pragma unroll
+            for (int p2 = 0; p2 < 2; ++p2) {
+              const uint32_t af[4] = {h0[p2], h0[p2 + 2], h8[p2], h8[p2 + 2]};
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) tc::mma_16816(oacc[2 * c + p2][nt], af, bw[nt][0], bw[nt][1]);
             }
-          } else {                              // unit = one chunk; one ldmatrix per unit pair
-            if ((u & 1) == 0) tc::ldsm_x4_trans(vc + vls[u / 2], r);
-            const int o = 2 * (u & 1);
-            uint32_t bp[4][2];
-            tc::q4_pairs<VAFF>(r[o], r[o + 1], bp);
-#pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) tc::mma_16816(oacc[u][s4], wa, bp[s4][0], bp[s4][1]);
           }
         }
       }
     }
-    // the slot is free once this warp (both warps of a pair) is done with it
-    if constexpr (DS == 2) {
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
-    } else {
-      __syncwarp();
-    }
-    if (producer && !timed_out && i + depth < n_local) issue(i + depth);
+    // the slot is free once every lane is done reading it: refill it with page k + D
+    __syncwarp();
+    if (k + D < n_local) issue(k + D, s);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    s = s + 1 == D ? 0 : s + 1;
   }
   tc::grid_dependents_launch();
 
-  // A wait that timed out: flag it, then give every issued copy of this group
-  // one more bounded wait so none is still writing the ring when it is reused.
-  if (timed_out) {
-    if (lane == 0) report(a.status, KVQ_DEV_TIMEOUT);
-    for (int i = max(0, n_local - depth); i < n_local; ++i)
-      tc::mbar_wait(gbar + 8 * (i % depth), (uint32_t)((i / depth) & 1));
-  }
+  // ---- merge the warps' states (shared memory reused once every warp is
+  // past its ring; no copies are pending)
   __syncthreads();
-
-  // ---- merge the warps' states (shared memory reused)
-  constexpr int NST = 4 / DS;
-  float* ows = reinterpret_cast<float*>(smem);   // [NST][G][HD]
-  float* mws = ows + NST * G * HD;               // [NST][G]
-  float* lws = mws + NST * G;                    // [NST][G]
-  const int state = warp / DS;
+  float* ows = reinterpret_cast<float*>(smem);   // [NW][G][HD]
+  float* mws = ows + NW * G * HD;                // [NW][G]
+  float* lws = mws + NW * G;                     // [NW][G]
 #pragma unroll
-  for (int u = 0; u < NU; ++u) {
-    float pbu = pb[u];
-    pbu += __shfl_xor_sync(0xffffffffu, pbu, 1);
-    pbu += __shfl_xor_sync(0xffffffffu, pbu, 2);
-    const float sc = vref[u] * (1.0f / kWScale);
-    if (live) {
+  for (int nt = 0; nt < NT; ++nt) {
+    float lt = l[nt];
+    lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+    float pbs[VNG];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        // 4-bit V: n-tiles 1 and 3 hold 16 * code
-        const float scj = (VK != KVQ_SYM_INT8 && (j & 1)) ? sc * (1.0f / 16.0f) : sc;
+    for (int g = 0; g < VNG; ++g) {
+      float v = pbias[nt][g];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      pbs[g] = v;
+    }
+    const int h = 4 * nt + tig;   // head owned by this lane (valid when < G)
+    if (h < G) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int d = dim0 + pv_dim<VK>(u, j, 2 * tig + e);
-          ows[(state * G + gid) * HD + d] = fmaf(oacc[u][j][e + 2], 1.0f / tc::kLoScale, oacc[u][j][e]) * scj + pbu;
+      for (int t = 0; t < MT; ++t) {
+        int d0, d1;
+        float f;
+        if constexpr (V8) {
+          d0 = 16 * t + 2 * gid;
+          d1 = d0 + 1;
+          f = 1.0f;
+        } else {
+          d0 = 32 * (t >> 1) + 4 * gid + (t & 1);
+          d1 = d0 + 2;
+          f = (t & 1) ? 1.0f / 16.0f : 1.0f;
         }
+        const int c = V8 ? t : (t >> 1);
+        const int g = ONEG ? 0 : ((VDC * c) >> A.v_group_shift);
+        float vi = vinv[0], pbg = pbs[0];
+#pragma unroll
+        for (int gg = 1; gg < VNG; ++gg)
+          if (gg == g) {
+            vi = vinv[gg];
+            pbg = pbs[gg];
+          }
+        const float sc = vi > 0.f ? f / vi : 0.f;   // R / 2^7, with 1/16 for 16 * code
+        ows[(w * G + h) * HD + d0] = fmaf(fmaf(oacc[t][nt][1], 1.0f / tc::kLoScale, oacc[t][nt][0]), sc, pbg);
+        ows[(w * G + h) * HD + d1] = fmaf(fmaf(oacc[t][nt][3], 1.0f / tc::kLoScale, oacc[t][nt][2]), sc, pbg);
+      }
+      if (gid == 0) {
+        mws[w * G + h] = m[nt];
+        lws[w * G + h] = lt;
       }
     }
-  }
-  if (tig == 0 && live && half == 0) {
-    mws[state * G + gid] = m;
-    lws[state * G + gid] = l;
   }
   __syncthreads();
 
   const int64_t cidx = ((int64_t)b * a.n_kv_heads + kvh) * a.n_chunks + chunk;
-  for (int i = tid; i < G * HD; i += kTcThreads) {
+  for (int i = tid; i < G * HD; i += NW * 32) {
     const int h = i / HD, d = i - h * HD;
     float M = mws[h];
 #pragma unroll
-    for (int st2 = 1; st2 < NST; ++st2) M = fmaxf(M, mws[st2 * G + h]);
+    for (int w2 = 1; w2 < NW; ++w2) M = fmaxf(M, mws[w2 * G + h]);
     float o = 0.f, ls = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int st2 = 0; st2 < NST; ++st2) {
-        const float f = exp2f(mws[st2 * G + h] - M);
-        o = fmaf(f, ows[(st2 * G + h) * HD + d], o);
-        ls = fmaf(f, lws[st2 * G + h], ls);
+      for (int w2 = 0; w2 < NW; ++w2) {
+        const float f = exp2f(mws[w2 * G + h] - M);
+        o = fmaf(f, ows[(w2 * G + h) * HD + d], o);
+        ls = fmaf(f, lws[w2 * G + h], ls);
       }
     }
     if (nch == 1) {
@@ -642,7 +700,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A, const __grid_constant__ CUten
   // 2^(m_c - M) / sum_c 2^(m_c - M) l_c per head in shared memory.
   float* wts = reinterpret_cast<float*>(smem);   // [nch][G] m, then weights
   float* lts = wts + nch * G;                    // [nch][G] l
-  for (int i = tid; i < nch * G; i += kTcThreads) {
+  for (int i = tid; i < nch * G; i += NW * 32) {
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml) + cbase * G + i);
     wts[i] = ml.x;
     lts[i] = ml.y;
@@ -654,9 +712,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A, const __grid_constant__ CUten
     float den = 0.f;
     for (int c = 0; c < nch; ++c) {
       const float mc = wts[c * G + tid];
-      const float w = (mx == -INFINITY || mc == -INFINITY) ? 0.f : exp2f(mc - mx);
-      wts[c * G + tid] = w;
-      den = fmaf(w, lts[c * G + tid], den);
+      const float wt = (mx == -INFINITY || mc == -INFINITY) ? 0.f : exp2f(mc - mx);
+      wts[c * G + tid] = wt;
+      den = fmaf(wt, lts[c * G + tid], den);
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     for (int c = 0; c < nch; ++c) wts[c * G + tid] *= inv;
@@ -665,7 +723,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A, const __grid_constant__ CUten
   // out = sum_c w_c acc_c: float4 loads, eight chunks in flight per thread
   const int NV4 = G * HD / 4;
   const float4* acc4 = reinterpret_cast<const float4*>(a.ws_acc) + cbase * NV4;
-  for (int e = tid; e < NV4; e += kTcThreads) {
+  for (int e = tid; e < NV4; e += NW * 32) {
     const int h = (4 * e) / HD;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     int c = 0;
@@ -675,20 +733,20 @@ decode_tc_kernel(const __grid_constant__ TcArgs A, const __grid_constant__ CUten
       for (int k = 0; k < 8; ++k) v[k] = __ldcg(acc4 + (int64_t)(c + k) * NV4 + e);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float w = wts[(c + k) * G + h];
-        o.x = fmaf(w, v[k].x, o.x);
-        o.y = fmaf(w, v[k].y, o.y);
-        o.z = fmaf(w, v[k].z, o.z);
-        o.w = fmaf(w, v[k].w, o.w);
+        const float wt = wts[(c + k) * G + h];
+        o.x = fmaf(wt, v[k].x, o.x);
+        o.y = fmaf(wt, v[k].y, o.y);
+        o.z = fmaf(wt, v[k].z, o.z);
+        o.w = fmaf(wt, v[k].w, o.w);
       }
     }
     for (; c < nch; ++c) {
       const float4 v = __ldcg(acc4 + (int64_t)c * NV4 + e);
-      const float w = wts[c * G + h];
-      o.x = fmaf(w, v.x, o.x);
-      o.y = fmaf(w, v.y, o.y);
-      o.z = fmaf(w, v.z, o.z);
-      o.w = fmaf(w, v.w, o.w);
+      const float wt = wts[c * G + h];
+      o.x = fmaf(wt, v.x, o.x);
+      o.y = fmaf(wt, v.y, o.y);
+      o.z = fmaf(wt, v.z, o.z);
+      o.w = fmaf(wt, v.w, o.w);
     }
     store_act(A.out, a.act, obase + 4 * e, o.x);
     store_act(A.out, a.act, obase + 4 * e + 1, o.y);
@@ -699,10 +757,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A, const __grid_constant__ CUten
 }
 
 // Host launcher of one instantiation (dynamic shared memory, optional PDL).
-template <int KK, int VK, int HD, bool ONEG, int PT>
-kvq_status launch_tc_one(const TcArgs& t, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid, size_t smem,
-                         cudaStream_t stream, bool pdl) {
-  auto kern = decode_tc_kernel<KK, VK, HD, ONEG, PT>;
+template <int KK, int VK, int HD, int NT, bool ONEG, int PT>
+kvq_status launch_tc_one(const TcArgs& t, dim3 grid, size_t smem, cudaStream_t stream, bool pdl) {
+  auto kern = decode_tc_kernel<KK, VK, HD, NT, ONEG, PT>;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -721,42 +778,47 @@ kvq_status launch_tc_one(const TcArgs& t, const CUtensorMap& mk, const CUtensorM
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, t, mk, mv);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, t);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }
 
+// Shapes with a tensor-core instantiation: head_dim 64 and 256 with G <= 4,
+// head_dim 128 with any G.
+inline bool tc_has_shape(int head_dim, int nt) {
+  return head_dim == 128 || ((head_dim == 64 || head_dim == 256) && nt == 1);
+}
+
 template <int KK, int VK, int PT>
-kvq_status launch_tc_pt(const TcArgs& t, const CUtensorMap& mk, const CUtensorMap& mv, int head_dim, bool oneg,
-                        dim3 grid, size_t smem, cudaStream_t stream, bool pdl) {
-#define KVQ_TC(HD_)                                                                               \
-  if (head_dim == HD_)                                                                            \
-    return oneg ? launch_tc_one<KK, VK, HD_, true, PT>(t, mk, mv, grid, smem, stream, pdl)        \
-                : launch_tc_one<KK, VK, HD_, false, PT>(t, mk, mv, grid, smem, stream, pdl);
-  KVQ_TC(64)
-  KVQ_TC(128)
-  if constexpr (KK != KVQ_SYM_INT8 && VK != KVQ_SYM_INT8) {   // 8-bit rows of 256 B have no TMA swizzle
-    KVQ_TC(256)
-  }
+kvq_status launch_tc_pt(const TcArgs& t, int head_dim, int nt, bool oneg, dim3 grid, size_t smem,
+                        cudaStream_t stream, bool pdl) {
+#define KVQ_TC(HD_, NT_)                                                                           \
+  if (head_dim == HD_ && nt == NT_)                                                                \
+    return oneg ? launch_tc_one<KK, VK, HD_, NT_, true, PT>(t, grid, smem, stream, pdl)            \
+                : launch_tc_one<KK, VK, HD_, NT_, false, PT>(t, grid, smem, stream, pdl);
+  KVQ_TC(64, 1)
+  KVQ_TC(128, 1)
+  KVQ_TC(128, 2)
+  KVQ_TC(256, 1)
 #undef KVQ_TC
   return fail(KVQ_ERR_UNSUPPORTED, "no tensor-core decode kernel for head_dim %d", head_dim);
 }
 
-template <int KK, int VK>
-kvq_status launch_tc_kinds(const TcArgs& t, const CUtensorMap& mk, const CUtensorMap& mv, int head_dim,
-                           bool oneg, int param, dim3 grid, size_t smem, cudaStream_t stream, bool pdl) {
-  if (param == KVQ_F32) return launch_tc_pt<KK, VK, KVQ_F32>(t, mk, mv, head_dim, oneg, grid, smem, stream, pdl);
-  if (param == KVQ_F16) return launch_tc_pt<KK, VK, KVQ_F16>(t, mk, mv, head_dim, oneg, grid, smem, stream, pdl);
-  return launch_tc_pt<KK, VK, KVQ_BF16>(t, mk, mv, head_dim, oneg, grid, smem, stream, pdl);
-}
-
-kvq_status launch_tc_s4s4(const TcArgs&, const CUtensorMap&, const CUtensorMap&, int, bool, int, dim3, size_t,
-                          cudaStream_t, bool);
-kvq_status launch_tc_s8s8(const TcArgs&, const CUtensorMap&, const CUtensorMap&, int, bool, int, dim3, size_t,
-                          cudaStream_t, bool);
-kvq_status launch_tc_s8s4(const TcArgs&, const CUtensorMap&, const CUtensorMap&, int, bool, int, dim3, size_t,
-                          cudaStream_t, bool);
-kvq_status launch_tc_a4a4(const TcArgs&, const CUtensorMap&, const CUtensorMap&, int, bool, int, dim3, size_t,
-                          cudaStream_t, bool);
+// One launcher per (K/V kind pair, scale type), each its own translation unit.
+typedef kvq_status (*TcLaunch)(const TcArgs&, int, int, bool, dim3, size_t, cudaStream_t, bool);
+#define KVQ_TC_DECLARE(NAME) kvq_status NAME(const TcArgs&, int, int, bool, dim3, size_t, cudaStream_t, bool);
+KVQ_TC_DECLARE(launch_tc_s4s4_f32)
+KVQ_TC_DECLARE(launch_tc_s4s4_f16)
+KVQ_TC_DECLARE(launch_tc_s4s4_bf16)
+KVQ_TC_DECLARE(launch_tc_s8s8_f32)
+KVQ_TC_DECLARE(launch_tc_s8s8_f16)
+KVQ_TC_DECLARE(launch_tc_s8s8_bf16)
+KVQ_TC_DECLARE(launch_tc_s8s4_f32)
+KVQ_TC_DECLARE(launch_tc_s8s4_f16)
+KVQ_TC_DECLARE(launch_tc_s8s4_bf16)
+KVQ_TC_DECLARE(launch_tc_a4a4_f32)
+KVQ_TC_DECLARE(launch_tc_a4a4_f16)
+KVQ_TC_DECLARE(launch_tc_a4a4_bf16)
+#undef KVQ_TC_DECLARE
 
 }  // namespace kvq

@@ -68,12 +68,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Wait for phase `phase` of the barrier for at most `limit_ns`; false on timeout.
+// Wait for phase `phase` of the barrier for at most `limit_ns` of
+// %globaltimer (a step of the timer backwards restarts the count); false on
+// timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint64_t limit_ns = 1000000000ull) {
   if (mbar_try_wait(bar, phase)) return true;
-  const uint64_t t0 = global_timer_ns();
+  uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, phase)) {
-    if (global_timer_ns() - t0 > limit_ns) return false;
+    const uint64_t t = global_timer_ns();
+    if (t < t0) t0 = t;
+    if (t - t0 > limit_ns) return false;
   }
   return true;
 }
