@@ -202,7 +202,8 @@ def whole_job(units_per_rank: float, world: int, ms_max: float) -> float:
 
 
 class BenchLayer:
-    def __init__(self, w: dict, window: bool, layer: int, device, gen, chunk_tokens: int = 0):
+    def __init__(self, w: dict, window: bool, layer: int, device, gen, chunk_tokens: int = 0,
+                 rope_tab=None):
         import torch
         from int8_quantized_paged_gb300 import kvq
         from int8_quantized_paged_gb300.cache import LayerCache
@@ -224,7 +225,8 @@ class BenchLayer:
             pool.alloc(n_pages)
             pool.free(wl.page_free_order(w, n_pages))
         rope_max = int(self.lens.max()) + 1
-        self.cache = LayerCache(cfg, self.B, max_pages, n_pages, rope_max, self.ring, device=device, pool=pool)
+        self.cache = LayerCache(cfg, self.B, max_pages, n_pages, rope_max, self.ring, device=device, pool=pool,
+                                rope_tab=rope_tab)
         for b, L in enumerate(self.lens):
             self.cache.reserve(b, self.ring if self.ring else int(L))
         self.cache.sync_table()
@@ -282,10 +284,16 @@ def run_gpu(args) -> dict | None:
     layers = []
     gen = torch.Generator(device=dev)
     gen.manual_seed(1000 + 97 * rank)
+    rope_tabs = {}   # one RoPE table per model: every layer reads the same positions
     for name, n, window in MODELS[args.workload]:
         w = wl.workload(name)
+        if name not in rope_tabs:
+            cfg = kvq.config(**w)
+            rows = int(wl.seq_lens(w).max()) + 1
+            rope_tabs[name] = (torch.from_numpy(kvq.rope_table(cfg, rows)).to(dev)
+                               if cfg.rope != kvq.ROPE_NONE else None)
         for i in range(n):
-            layers.append(BenchLayer(w, window, len(layers), dev, gen, args.chunk_tokens))
+            layers.append(BenchLayer(w, window, len(layers), dev, gen, args.chunk_tokens, rope_tabs[name]))
     torch.cuda.synchronize()
     for L in layers:
         assert L.cache.status_bits() == 0, "prefill flagged a bad page or position"

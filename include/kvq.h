@@ -237,7 +237,8 @@ kvq_status kvq_append(const kvq_config* cfg, int32_t n_rows,
  * fp32 online softmax (m, l, acc), and the last chunk of each (sequence, kv
  * head) to finish merges the chunks with log-sum-exp weights.  fp32 softmax:
  * [airllm] §3.4.
- *   q, out        device [batch][n_heads][head_dim] of act_dtype
+ *   q, out        device [batch][n_heads][head_dim] of act_dtype; q 16-byte
+ *                 aligned (KVQ_ERR_INVALID_ARG otherwise)
  *   seq_lens      device int32 [batch], 0 <= L <= max_pages_per_seq*page_size
  *   chunk_tokens  0: the library chooses; else a multiple of page_size
  *   workspace     device scratch of at least kvq_decode_workspace_bytes()

@@ -17,7 +17,7 @@ _TORCH_ACT = {kvq.F32: torch.float32, kvq.F16: torch.float16, kvq.BF16: torch.bf
 class LayerCache:
     def __init__(self, cfg: kvq.Config, n_seqs: int, max_pages_per_seq: int, n_pool_pages: int,
                  rope_max_pos: int = 0, ring_rows: int = 0, device="cuda", pool: kvq.Pool | None = None,
-                 rope_host: np.ndarray | None = None):
+                 rope_host: np.ndarray | None = None, rope_tab: torch.Tensor | None = None):
         self.cfg = cfg
         self.device = torch.device(device)
         self.n_seqs, self.max_pages, self.n_pool_pages = n_seqs, max_pages_per_seq, n_pool_pages
@@ -31,8 +31,13 @@ class LayerCache:
         self.rope_max_pos = rope_max_pos
         self.rope_tab = None
         if cfg.rope != kvq.ROPE_NONE and rope_max_pos > 0:
-            host = rope_host if rope_host is not None else kvq.rope_table(cfg, rope_max_pos)
-            self.rope_tab = torch.from_numpy(host).to(self.device)
+            if rope_tab is not None:   # a table shared by the layers of a model
+                if rope_tab.shape[0] < rope_max_pos:
+                    raise ValueError("shared RoPE table has fewer rows than rope_max_pos")
+                self.rope_tab = rope_tab
+            else:
+                host = rope_host if rope_host is not None else kvq.rope_table(cfg, rope_max_pos)
+                self.rope_tab = torch.from_numpy(host).to(self.device)
 
     @property
     def act_dtype(self) -> torch.dtype:

@@ -112,6 +112,11 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendArgs a) {
   constexpr int DPL = HD / 32;
   constexpr int P = 16;
   const int lane = threadIdx.x & 31;
+  // Programmatic dependent launch: the new rows may come from the kernel
+  // before this one; the kernel after it may start launching at once (it
+  // waits for this grid before reading the pools).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (item >= (int64_t)a.n_rows * a.n_kv_heads) return;
   const int row = (int)(item / a.n_kv_heads);
@@ -218,14 +223,24 @@ extern "C" kvq_status kvq_append(const kvq_config* cfg, int32_t n_rows, const vo
   const int64_t warps = (int64_t)n_rows * cfg->n_kv_heads;
   const int64_t blocks = (warps + 3) / 4;
   if (blocks > 0x7fffffffLL) return fail(KVQ_ERR_INVALID_ARG, "too many rows");
-  cudaStream_t s = (cudaStream_t)stream;
+  if (blocks == 0) return KVQ_OK;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)blocks);
+  lc.blockDim = dim3(128);
+  lc.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaError_t e;
   switch (cfg->head_dim) {
-    case 64: append_kernel<64><<<(unsigned)blocks, 128, 0, s>>>(a); break;
-    case 128: append_kernel<128><<<(unsigned)blocks, 128, 0, s>>>(a); break;
-    case 256: append_kernel<256><<<(unsigned)blocks, 128, 0, s>>>(a); break;
+    case 64: e = cudaLaunchKernelEx(&lc, append_kernel<64>, a); break;
+    case 128: e = cudaLaunchKernelEx(&lc, append_kernel<128>, a); break;
+    case 256: e = cudaLaunchKernelEx(&lc, append_kernel<256>, a); break;
     default: return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d", cfg->head_dim);
   }
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }

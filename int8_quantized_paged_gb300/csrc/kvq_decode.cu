@@ -48,15 +48,6 @@ static int tc_resident(const kvq_config& c) {
   return tc_min_blocks(c.head_dim, G > 4 ? 2 : 1);
 }
 
-static bool pdl_enabled() {
-  static int on = -1;
-  if (on < 0) {
-    const char* e = std::getenv("KVQ_PDL");
-    on = (e && std::strcmp(e, "0") == 0) ? 0 : 1;
-  }
-  return on != 0;
-}
-
 // Chunking and workspace layout of one decode call.  The workspace holds, in
 // order: arrival counters [batch][n_kv_heads] (int32, zero between calls),
 // partial sums acc [batch][n_kv_heads][n_chunks][G][head_dim] and partial
@@ -84,13 +75,14 @@ static Plan make_plan(const kvq_config& c, int32_t batch, int64_t max_tokens, bo
     p.blocks_per_chunk = requested / P;
   } else {
     // About whole waves of resident CTAs, assuming every sequence is as long
-    // as the longest, and at most 128 blocks per chunk.
+    // as the longest, with 16 to 128 blocks per chunk: at least four pages
+    // per warp, so a short context does not split into many small partials.
     const int64_t total = (int64_t)batch * c.n_kv_heads * max_blocks;
     const int64_t wave = (int64_t)num_sms() * tc_resident(c);
     const int64_t waves = (total + wave * 128 - 1) / (wave * 128);
     int64_t cb = (total + waves * wave - 1) / (waves * wave);
     cb = (cb + kWarps - 1) / kWarps * kWarps;
-    p.blocks_per_chunk = (int)(cb < 2 * kWarps ? 2 * kWarps : (cb > 128 ? 128 : cb));
+    p.blocks_per_chunk = (int)(cb < 4 * kWarps ? 4 * kWarps : (cb > 128 ? 128 : cb));
   }
   const int64_t n_tc = (max_blocks + p.blocks_per_chunk - 1) / p.blocks_per_chunk;
   p.tc_chunks = (int)(n_tc < 1 ? 1 : (n_tc > (1 << 30) ? (1 << 30) : n_tc));
@@ -218,7 +210,9 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
       return fail(KVQ_ERR_UNSUPPORTED, "scale rows larger than the tensor-core kernel's slots");
     size_t smem = (size_t)kWarps * tc_depth(cfg->head_dim, nt) * tc_slot_bytes(k, v, cfg->head_dim, oneg, pt);
     const size_t need_merge = (size_t)kWarps * G * (cfg->head_dim + 2) * sizeof(float);
-    const size_t need_comb = (size_t)w.n_chunks * G * 2 * sizeof(float);
+    // combine: (m, l) of every chunk, then the per-group column sums
+    const size_t need_comb = (size_t)w.n_chunks * G * 2 * sizeof(float) + 16 +
+                             (size_t)kTcThreads * 4 * sizeof(float);
     if (smem < need_merge) smem = need_merge;
     if (smem < need_comb) smem = need_comb;
     if (smem > 200 * 1024)
@@ -274,6 +268,7 @@ static kvq_status check_decode_args(const kvq_config* cfg, int32_t batch, const 
     return fail(KVQ_ERR_INVALID_ARG, "RoPE config needs rope_tab and rope_max_pos >= 1");
   if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool)) & 15)
     return fail(KVQ_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(q) & 15) return fail(KVQ_ERR_INVALID_ARG, "q must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(workspace) & 255)
     return fail(KVQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   return KVQ_OK;

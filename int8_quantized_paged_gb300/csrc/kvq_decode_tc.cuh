@@ -118,6 +118,44 @@ __host__ __device__ constexpr int tc_slot_bytes(int kk, int vk, int hd, bool one
          tc_scale_bytes(kk, hd, oneg, pt) + tc_scale_bytes(vk, hd, oneg, pt);
 }
 
+// N consecutive activation elements (f32 / f16 / bf16) from element `off` of
+// `p`, with vector loads; `off` is a multiple of N and the base 16-byte aligned.
+template <int N>
+__device__ __forceinline__ void load_run(const void* p, int act, int64_t off, float (&v)[N]) {
+  static_assert(N == 4 || N == 8, "run");
+  if (act == KVQ_F32) {
+    const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(p) + off);
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      const float4 x = s[i];
+      v[4 * i] = x.x;
+      v[4 * i + 1] = x.y;
+      v[4 * i + 2] = x.z;
+      v[4 * i + 3] = x.w;
+    }
+  } else {
+    uint32_t u[N / 2];
+    const unsigned short* s = static_cast<const unsigned short*>(p) + off;
+    if constexpr (N == 8) {
+      const uint4 x = *reinterpret_cast<const uint4*>(s);
+      u[0] = x.x; u[1] = x.y; u[2] = x.z; u[3] = x.w;
+    } else {
+      const uint2 x = *reinterpret_cast<const uint2*>(s);
+      u[0] = x.x; u[1] = x.y;
+    }
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      if (act == KVQ_F16) {
+        v[2 * i] = __half2float(__ushort_as_half((unsigned short)(u[i] & 0xFFFFu)));
+        v[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(u[i] >> 16)));
+      } else {
+        v[2 * i] = __uint_as_float(u[i] << 16);
+        v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
 // (hi, lo) fp16 parts of x packed as (low half, high half): x = hi + lo * 2^-12.
 __device__ __forceinline__ uint32_t hilo_pack(float x) {
   const float hi = __half2float(__float2half_rn(x));
@@ -171,11 +209,34 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   const int gid = lane >> 2, tig = lane & 3;
 
   tc::grid_dependency_wait();   // inputs may come from the kernel before this one
+  // Kernels launched after this one may start their launch now; each waits
+  // for this grid to finish before it reads anything it writes.
+  tc::grid_dependents_launch();
 
+  // One round of independent loads: the length, this lane's raw q elements
+  // (see the fragments below) and, for a whole-context decode, the block-table
+  // entries of the warp's pages, which do not depend on the length.
+  const int64_t obase = ((int64_t)b * a.n_heads + (int64_t)kvh * G) * HD;
   const int L = a.seq_lens[b];
+  float qv[NT][KCH][RUN];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hq = NT == 1 ? (gid >> 1) % G : 4 * nt + (gid >> 1);
+#pragma unroll
+    for (int c = 0; c < KCH; ++c) load_run<RUN>(a.q, a.act, obase + (int64_t)hq * HD + KDC * c + RUN * tig, qv[nt][c]);
+  }
+  const int CB = A.blocks_per_chunk;
+  const int w = warp;
+  const int32_t* bt = a.block_table + (int64_t)b * a.max_pages;
+  const bool whole = a.window == 0 && a.ring_rows == 0;
+  int ids = -1;   // page ids of this warp's pages 32q .. 32q+31 (lane k % 32)
+  if (whole) {
+    const int blk = chunk * CB + w + NW * lane;
+    if (blk < a.max_pages) ids = bt[blk];
+  }
+
   int lo = 0, bad = 0;
   const int n_att = attended(a, L, &lo, &bad);
-  const int64_t obase = ((int64_t)b * a.n_heads + (int64_t)kvh * G) * HD;
   if (n_att <= 0) {
     if (chunk == 0) {
       if (bad && tid == 0 && kvh == 0) report(a.status, bad);
@@ -183,13 +244,11 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     }
     return;
   }
-  const int CB = A.blocks_per_chunk;
   const int blk_lo = lo / P, blk_hi = (L + P - 1) / P;
   const int nch = (blk_hi - blk_lo + CB - 1) / CB;
   if (chunk >= nch) return;
   const int cb0 = blk_lo + chunk * CB;
   const int ncb = min(CB, blk_hi - cb0);
-  const int w = warp;
   const int n_local = w < ncb ? (ncb - w + NW - 1) / NW : 0;   // pages w, w + NW, ... of the chunk
 
   // ---- page ring of this warp: D slots of SLOT bytes.  Lane (hl = lane % 16)
@@ -209,23 +268,25 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     else d = j < VC / 16 ? KC + swz<VRB>(j / VCH, j % VCH) : KC + VC + KPMAX + 16 * (j - VC / 16);
     cp_dst[m] = wring + d;
   }
-  const int32_t* bt = a.block_table + (int64_t)b * a.max_pages;
   const int ring = a.ring_rows, npp = a.n_pool_pages;
-  auto page_of = [&](int k) -> int {   // page id of this warp's k-th page, -1 if unreadable
+  auto page_of = [&](int k) -> int {   // page id of this warp's k-th page (k < n_local)
     const int blk = cb0 + w + NW * k;
     const int idx = ring > 0 ? (int)(((int64_t)blk * P) % ring) / P : blk;
-    const int pg = bt[idx];
+    return bt[idx];
+  };
+  auto checked = [&](int pg, int k) -> int {   // -1 (and a flag) for an id outside the pool
     const bool ok = pg >= 0 && pg < npp;
-    if (!ok) report(a.status, KVQ_DEV_BAD_PAGE);
+    if (!ok && k < n_local) report(a.status, KVQ_DEV_BAD_PAGE);
     return ok ? pg : -1;
   };
   const uint8_t* pool_lane = (vlane ? a.v_pool + (int64_t)kvh * a.vl.sub_bytes
                                     : a.k_pool + (int64_t)kvh * a.kl.sub_bytes) + 16 * hl;
   const int64_t page_lane = vlane ? a.vl.page_bytes : a.kl.page_bytes;
-  int ids = n_local > 0 ? page_of(min(lane, n_local - 1)) : -1;   // page ids of pages 32q .. 32q+31
-  uint32_t valid = 0;                                               // bit s: slot s holds a page
+  if (!whole && lane < n_local) ids = page_of(lane);
+  ids = checked(ids, lane);
+  uint32_t valid = 0;   // bit s: slot s holds a page
   auto issue = [&](int k, int s) {   // all lanes: copies of page k into slot s
-    if ((k & 31) == 0 && k > 0) ids = page_of(min(k + lane, n_local - 1));
+    if ((k & 31) == 0 && k > 0) ids = checked(k + lane < n_local ? page_of(k + lane) : -1, k + lane);
     const int pg = __shfl_sync(0xffffffffu, ids, k & 31);
     valid = pg >= 0 ? (valid | (1u << s)) : (valid & ~(1u << s));
     if (pg < 0) return;
@@ -251,25 +312,18 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     const int part = gid & 1;
     const float2* cs = reinterpret_cast<const float2*>(a.rope_tab) + (int64_t)(L - 1) * (HD / 2);
     const float sc = a.score_scale * kQScale;
-    const int rope = a.rope, act = a.act;
+    const int rope = a.rope;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int hq = NT == 1 ? (gid >> 1) % G : 4 * nt + (gid >> 1);
-      const int64_t qoff = obase + (int64_t)hq * HD;
-      float qv[KCH][RUN];
-#pragma unroll
-      for (int c = 0; c < KCH; ++c)
-#pragma unroll
-        for (int k = 0; k < RUN; ++k) qv[c][k] = load_act(a.q, act, qoff + KDC * c + RUN * tig + k);
       if (rope == KVQ_ROPE_NORMAL) {   // pairs (2i, 2i+1) lie inside a run
 #pragma unroll
         for (int c = 0; c < KCH; ++c)
 #pragma unroll
           for (int k = 0; k < RUN; k += 2) {
             const float2 t = cs[(KDC * c + RUN * tig + k) >> 1];
-            const float x0 = qv[c][k], x1 = qv[c][k + 1];
-            qv[c][k] = x0 * t.x - x1 * t.y;
-            qv[c][k + 1] = x0 * t.y + x1 * t.x;
+            const float x0 = qv[nt][c][k], x1 = qv[nt][c][k + 1];
+            qv[nt][c][k] = x0 * t.x - x1 * t.y;
+            qv[nt][c][k + 1] = x0 * t.y + x1 * t.x;
           }
       } else if (rope == KVQ_ROPE_NEOX) {   // pairs (i, i + HD/2): chunk c with chunk c + KCH/2
 #pragma unroll
@@ -277,31 +331,31 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 #pragma unroll
           for (int k = 0; k < RUN; ++k) {
             const float2 t = cs[KDC * c + RUN * tig + k];
-            const float x0 = qv[c][k], x1 = qv[c + KCH / 2][k];
-            qv[c][k] = x0 * t.x - x1 * t.y;
-            qv[c + KCH / 2][k] = x0 * t.y + x1 * t.x;
+            const float x0 = qv[nt][c][k], x1 = qv[nt][c + KCH / 2][k];
+            qv[nt][c][k] = x0 * t.x - x1 * t.y;
+            qv[nt][c + KCH / 2][k] = x0 * t.y + x1 * t.x;
           }
       }
 #pragma unroll
       for (int c = 0; c < KCH; ++c)
 #pragma unroll
-        for (int k = 0; k < RUN; ++k) qv[c][k] *= sc;
+        for (int k = 0; k < RUN; ++k) qv[nt][c][k] *= sc;
       // B fragments: 4-bit K chunk c, parity p (p = 1 meets 16 * code, so q / 16):
       //   b0 = q at dims KDC*c + 8tig + p + {0, 4},  b1 = dims + {2, 6}
       // 8-bit K chunk c:  b0 = dims 16c + 4tig + {0, 2},  b1 = dims + {1, 3}
 #pragma unroll
       for (int c = 0; c < KCH; ++c) {
         if constexpr (K8) {
-          qb[nt][c][0] = tc::pack_half2(hilo_part(qv[c][0], part), hilo_part(qv[c][2], part));
-          qb[nt][c][1] = tc::pack_half2(hilo_part(qv[c][1], part), hilo_part(qv[c][3], part));
+          qb[nt][c][0] = tc::pack_half2(hilo_part(qv[nt][c][0], part), hilo_part(qv[nt][c][2], part));
+          qb[nt][c][1] = tc::pack_half2(hilo_part(qv[nt][c][1], part), hilo_part(qv[nt][c][3], part));
         } else {
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             const float f = p ? 1.0f / 16.0f : 1.0f;
             qb[nt][2 * c + p][0] =
-                tc::pack_half2(hilo_part(qv[c][p] * f, part), hilo_part(qv[c][p + 4] * f, part));
+                tc::pack_half2(hilo_part(qv[nt][c][p] * f, part), hilo_part(qv[nt][c][p + 4] * f, part));
             qb[nt][2 * c + p][1] =
-                tc::pack_half2(hilo_part(qv[c][p + 2] * f, part), hilo_part(qv[c][p + 6] * f, part));
+                tc::pack_half2(hilo_part(qv[nt][c][p + 2] * f, part), hilo_part(qv[nt][c][p + 6] * f, part));
           }
         }
       }
@@ -319,7 +373,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
           for (int gg = 0; gg < KNG; ++gg)
             if (gg == g)
 #pragma unroll
-              for (int k = 0; k < RUN; ++k) part_sum[gg] += qv[c][k];
+              for (int k = 0; k < RUN; ++k) part_sum[gg] += qv[nt][c][k];
         }
 #pragma unroll
         for (int g = 0; g < KNG; ++g) {
@@ -601,7 +655,6 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     asm volatile("cp.async.commit_group;" ::: "memory");
     s = s + 1 == D ? 0 : s + 1;
   }
-  tc::grid_dependents_launch();
 
   // ---- merge the warps' states (shared memory reused once every warp is
   // past its ring; no copies are pending)
@@ -696,51 +749,73 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   if (!flag_s) return;
   __threadfence();
   const int64_t cbase = ((int64_t)b * a.n_kv_heads + kvh) * a.n_chunks;
-  // (m, l) of every chunk and head in one parallel round, then the weights
-  // 2^(m_c - M) / sum_c 2^(m_c - M) l_c per head in shared memory.
-  float* wts = reinterpret_cast<float*>(smem);   // [nch][G] m, then weights
-  float* lts = wts + nch * G;                    // [nch][G] l
-  for (int i = tid; i < nch * G; i += NW * 32) {
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml) + cbase * G + i);
-    wts[i] = ml.x;
-    lts[i] = ml.y;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float mx = -INFINITY;
-    for (int c = 0; c < nch; ++c) mx = fmaxf(mx, wts[c * G + tid]);
-    float den = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const float mc = wts[c * G + tid];
-      const float wt = (mx == -INFINITY || mc == -INFINITY) ? 0.f : exp2f(mc - mx);
-      wts[c * G + tid] = wt;
-      den = fmaf(wt, lts[c * G + tid], den);
+  // Weights 2^(m_c - M) / sum_c 2^(m_c - M) l_c per head into shared memory:
+  // warp w takes heads w, w + NW, ...; its lanes hold chunks lane + 32 i
+  // (up to 4 per lane in registers, later ones are read again).
+  float* wts = reinterpret_cast<float*>(smem);   // [nch][G]
+  const float2* mlp = reinterpret_cast<const float2*>(a.ws_ml) + cbase * G;
+  for (int h = w; h < G; h += NW) {
+    float2 ml[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = lane + 32 * i;
+      ml[i] = c < nch ? __ldcg(mlp + (int64_t)c * G + h) : make_float2(-INFINITY, 0.f);
     }
+    float mx = fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x));
+    for (int c = lane + 128; c < nch; c += 32) mx = fmaxf(mx, __ldcg(mlp + (int64_t)c * G + h).x);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float den = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float wt = (mx == -INFINITY || ml[i].x == -INFINITY) ? 0.f : exp2f(ml[i].x - mx);
+      ml[i].x = wt;
+      den = fmaf(wt, ml[i].y, den);
+    }
+    for (int c = lane + 128; c < nch; c += 32) {
+      const float2 v = __ldcg(mlp + (int64_t)c * G + h);
+      const float wt = (mx == -INFINITY || v.x == -INFINITY) ? 0.f : exp2f(v.x - mx);
+      wts[c * G + h] = wt;
+      den = fmaf(wt, v.y, den);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int c = 0; c < nch; ++c) wts[c * G + tid] *= inv;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nch) wts[c * G + h] = ml[i].x * inv;
+    }
+    for (int c = lane + 128; c < nch; c += 32) wts[c * G + h] *= inv;
   }
   __syncthreads();
-  // out = sum_c w_c acc_c: float4 loads, eight chunks in flight per thread
+  // out = sum_c w_c acc_c.  The float4 columns of the partials are spread over
+  // the threads, and when there are fewer columns than threads the chunks are
+  // split into NGRP groups summed separately, then added through shared memory.
+  // Each thread keeps up to 16 partial loads in flight.
   const int NV4 = G * HD / 4;
+  const int NGRP = NV4 >= kTcThreads ? 1 : kTcThreads / NV4;
   const float4* acc4 = reinterpret_cast<const float4*>(a.ws_acc) + cbase * NV4;
-  for (int e = tid; e < NV4; e += NW * 32) {
+  float4* red = reinterpret_cast<float4*>(smem + ((8 * nch * G + 15) & ~15));   // [NGRP][NV4], 16-byte aligned
+  for (int t = tid; t < NV4 * NGRP; t += kTcThreads) {
+    const int e = t % NV4, grp = t / NV4;
     const int h = (4 * e) / HD;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    int c = 0;
-    for (; c + 8 <= nch; c += 8) {
-      float4 v[8];
+    int c = grp;
+    for (; c + 15 * NGRP < nch; c += 16 * NGRP) {
+      float4 v[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = __ldcg(acc4 + (int64_t)(c + k) * NV4 + e);
+      for (int k = 0; k < 16; ++k) v[k] = __ldcg(acc4 + (int64_t)(c + k * NGRP) * NV4 + e);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float wt = wts[(c + k) * G + h];
+      for (int k = 0; k < 16; ++k) {
+        const float wt = wts[(c + k * NGRP) * G + h];
         o.x = fmaf(wt, v[k].x, o.x);
         o.y = fmaf(wt, v[k].y, o.y);
         o.z = fmaf(wt, v[k].z, o.z);
         o.w = fmaf(wt, v[k].w, o.w);
       }
     }
-    for (; c < nch; ++c) {
+    for (; c < nch; c += NGRP) {
       const float4 v = __ldcg(acc4 + (int64_t)c * NV4 + e);
       const float wt = wts[c * G + h];
       o.x = fmaf(wt, v.x, o.x);
@@ -748,10 +823,31 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       o.z = fmaf(wt, v.z, o.z);
       o.w = fmaf(wt, v.w, o.w);
     }
-    store_act(A.out, a.act, obase + 4 * e, o.x);
-    store_act(A.out, a.act, obase + 4 * e + 1, o.y);
-    store_act(A.out, a.act, obase + 4 * e + 2, o.z);
-    store_act(A.out, a.act, obase + 4 * e + 3, o.w);
+    if (NGRP == 1) {
+      store_act(A.out, a.act, obase + 4 * e, o.x);
+      store_act(A.out, a.act, obase + 4 * e + 1, o.y);
+      store_act(A.out, a.act, obase + 4 * e + 2, o.z);
+      store_act(A.out, a.act, obase + 4 * e + 3, o.w);
+    } else {
+      red[grp * NV4 + e] = o;
+    }
+  }
+  if (NGRP > 1) {
+    __syncthreads();
+    for (int e = tid; e < NV4; e += kTcThreads) {
+      float4 o = red[e];
+      for (int g2 = 1; g2 < NGRP; ++g2) {
+        const float4 x = red[g2 * NV4 + e];
+        o.x += x.x;
+        o.y += x.y;
+        o.z += x.z;
+        o.w += x.w;
+      }
+      store_act(A.out, a.act, obase + 4 * e, o.x);
+      store_act(A.out, a.act, obase + 4 * e + 1, o.y);
+      store_act(A.out, a.act, obase + 4 * e + 2, o.z);
+      store_act(A.out, a.act, obase + 4 * e + 3, o.w);
+    }
   }
   if (tid == 0) *counter = 0;   // ready for the next call
 }

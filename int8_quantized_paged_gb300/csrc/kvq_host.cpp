@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -122,6 +123,15 @@ int num_sms() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+bool pdl_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char* e = std::getenv("KVQ_PDL");
+    on = (e && std::strcmp(e, "0") == 0) ? 0 : 1;
+  }
+  return on != 0;
 }
 
 int chunk_tokens_for(const kvq_config& c, int32_t batch, int64_t max_tokens, int32_t requested) {

@@ -49,6 +49,10 @@ float score_scale_log2(const kvq_config& c);
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 
+// Whether kernels are launched with programmatic dependent launch (set
+// KVQ_PDL=0 in the environment to turn it off).
+bool pdl_enabled();
+
 // Number of chunks a sequence of up to max_tokens attended tokens is split into.
 int chunk_tokens_for(const kvq_config& c, int32_t batch, int64_t max_tokens,
                      int32_t requested);
