@@ -39,7 +39,7 @@ static bool tc_enabled(const kvq_config& c) {
   const bool pow2 = (c.k_group & (c.k_group - 1)) == 0 && (c.v_group & (c.v_group - 1)) == 0;
   if (!pow2 || c.k_param_dtype != c.v_param_dtype || c.k_group < 32 || c.v_group < 32) return false;
   const int G = c.n_heads / c.n_kv_heads;
-  return tc_has_shape(c.head_dim, G > 4 ? 2 : 1);
+  return c.k_group == c.v_group && tc_has_shape(c.head_dim, G > 4 ? 2 : 1, c.head_dim / c.k_group);
 }
 
 // CTAs of the tensor-core kernel resident per SM (its launch bounds).
@@ -195,8 +195,6 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     t.counters = static_cast<int32_t*>(workspace);
     t.G = G;
     t.blocks_per_chunk = w.blocks_per_chunk;
-    t.k_group_shift = __builtin_ctz((unsigned)cfg->k_group);
-    t.v_group_shift = __builtin_ctz((unsigned)cfg->v_group);
     t.kc_bytes = cfg->page_size * a.kl.code_bytes;
     t.vc_bytes = cfg->page_size * a.vl.code_bytes;
     t.kp_bytes = cfg->page_size * a.kl.param_row_bytes;
@@ -204,11 +202,11 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     // Shared memory: a ring of tc_depth pages per warp, reused at the end for
     // the warps' merge and the combine weights.
     const int nt = G > 4 ? 2 : 1;
-    const bool oneg = cfg->k_group >= cfg->head_dim && cfg->v_group >= cfg->head_dim;
+    const int ng = cfg->head_dim / cfg->k_group;   // scale groups per head (K and V alike)
     const int pt = cfg->k_param_dtype;
-    if (t.kp_bytes > tc_scale_bytes(k, cfg->head_dim, oneg, pt) || t.vp_bytes > tc_scale_bytes(v, cfg->head_dim, oneg, pt))
-      return fail(KVQ_ERR_UNSUPPORTED, "scale rows larger than the tensor-core kernel's slots");
-    size_t smem = (size_t)kWarps * tc_depth(cfg->head_dim, nt) * tc_slot_bytes(k, v, cfg->head_dim, oneg, pt);
+    if (t.kp_bytes != tc_scale_bytes(k, ng, pt) || t.vp_bytes != tc_scale_bytes(v, ng, pt))
+      return fail(KVQ_ERR_UNSUPPORTED, "scale rows do not match the tensor-core kernel's slots");
+    size_t smem = (size_t)kWarps * tc_depth(cfg->head_dim, nt) * tc_slot_bytes(k, v, cfg->head_dim, ng, pt);
     const size_t need_merge = (size_t)kWarps * G * (cfg->head_dim + 2) * sizeof(float);
     // combine: (m, l) of every chunk, then the per-group column sums
     const size_t need_comb = (size_t)w.n_chunks * G * 2 * sizeof(float) + 16 +
@@ -230,7 +228,7 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
                      : (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT8) ? 1
                      : (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT4) ? 2
                                                                 : 3;
-    st = table[kind][cfg->k_param_dtype](t, hd, nt, oneg, grid, smem, stream, pdl);
+    st = table[kind][cfg->k_param_dtype](t, hd, nt, ng, grid, smem, stream, pdl);
     return st;
   }
 

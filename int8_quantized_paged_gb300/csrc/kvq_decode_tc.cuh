@@ -65,7 +65,6 @@ struct TcArgs {
   int32_t G;                 // query heads per kv head (1..8)
   int32_t blocks_per_chunk;  // 16-token blocks per chunk
   int32_t kc_bytes, vc_bytes, kp_bytes, vp_bytes;  // code and scale bytes of a page (one kv head)
-  int32_t k_group_shift, v_group_shift;            // log2 of the group sizes
 };
 
 constexpr int kWarps = 4;
@@ -108,14 +107,13 @@ __device__ __forceinline__ float ld_param(uint32_t addr) {
   }
 }
 
-// Upper bound of the scale (and bias) bytes of one page of one kv head: one
-// group per head when ONEG, else groups of at least 32 elements.
-__host__ __device__ constexpr int tc_scale_bytes(int kind, int hd, bool oneg, int pt) {
-  return 16 * (oneg ? 1 : hd / 32) * (kind == KVQ_AFFINE_INT4 ? 2 : 1) * (pt == KVQ_F32 ? 4 : 2);
+// Scale (and bias) bytes of one page of one kv head with ng groups per head.
+__host__ __device__ constexpr int tc_scale_bytes(int kind, int ng, int pt) {
+  return 16 * ng * (kind == KVQ_AFFINE_INT4 ? 2 : 1) * (pt == KVQ_F32 ? 4 : 2);
 }
-__host__ __device__ constexpr int tc_slot_bytes(int kk, int vk, int hd, bool oneg, int pt) {
+__host__ __device__ constexpr int tc_slot_bytes(int kk, int vk, int hd, int ng, int pt) {
   return 16 * (kk == KVQ_SYM_INT8 ? hd : hd / 2) + 16 * (vk == KVQ_SYM_INT8 ? hd : hd / 2) +
-         tc_scale_bytes(kk, hd, oneg, pt) + tc_scale_bytes(vk, hd, oneg, pt);
+         tc_scale_bytes(kk, ng, pt) + tc_scale_bytes(vk, ng, pt);
 }
 
 // N consecutive activation elements (f32 / f16 / bf16) from element `off` of
@@ -169,9 +167,10 @@ __device__ __forceinline__ float hilo_part(float x, int part) {
 }
 
 // KK / VK: code kinds of K and V.  HD: head dim.  NT: 8-column tiles (1 for
-// G <= 4, 2 for G = 8).  ONEG: one K group and one V group span the head.
+// G <= 4, 2 for G = 8).  NG: scale groups per head (the same for K and V),
+// so every group index below is a compile-time constant.
 // PT: stored type of the scales (and biases) of K and V.
-template <int KK, int VK, int HD, int NT, bool ONEG, int PT>
+template <int KK, int VK, int HD, int NT, int NG, int PT>
 __global__ void __launch_bounds__(kTcThreads, tc_min_blocks(HD, NT))
 decode_tc_kernel(const __grid_constant__ TcArgs A) {
   constexpr int P = 16;
@@ -189,11 +188,12 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   constexpr int MT = HD / 16;                    // P.V m-tiles
   constexpr int RUN = K8 ? 4 : 8;                // contiguous q dims a lane holds per K chunk
   constexpr int PB = PT == KVQ_F32 ? 4 : 2;      // bytes of a stored scale
-  constexpr int KNG = ONEG ? 1 : HD / 32;        // K groups held (upper bound when !ONEG)
-  constexpr int VNG = ONEG ? 1 : HD / 32;
+  constexpr bool ONEG = NG == 1;
+  constexpr int GS = HD / NG;                    // dims per scale group
+  constexpr int KNG = NG, VNG = NG;
   // Ring slot: [K codes KC][V codes VC][K scales <= KPMAX][V scales <= VPMAX]
   constexpr int KC = 16 * KRB, VC = 16 * VRB;
-  constexpr int KPMAX = tc_scale_bytes(KK, HD, ONEG, PT), VPMAX = tc_scale_bytes(VK, HD, ONEG, PT);
+  constexpr int KPMAX = tc_scale_bytes(KK, NG, PT), VPMAX = tc_scale_bytes(VK, NG, PT);
   constexpr int SLOT = KC + VC + KPMAX + VPMAX;
   // 16-byte copies per lane and page: lanes 0-15 copy the K sub-block, 16-31 the V one
   constexpr int NCP = cmax((KC + KPMAX) / 16, (VC + VPMAX) / 16) / 16 + 1;
@@ -368,7 +368,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         for (int g = 0; g < KNG; ++g) part_sum[g] = 0.f;
 #pragma unroll
         for (int c = 0; c < KCH; ++c) {
-          const int g = ONEG ? 0 : ((KDC * c) >> A.k_group_shift);
+          const int g = (KDC * c) / GS;
 #pragma unroll
           for (int gg = 0; gg < KNG; ++gg)
             if (gg == g)
@@ -501,7 +501,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
             }
           }
           if constexpr (!ONEG) {
-            if (((KDC * (c + 1)) & ((1 << A.k_group_shift) - 1)) == 0) fold((KDC * c) >> A.k_group_shift);
+            if ((KDC * (c + 1)) % GS == 0) fold((KDC * c) / GS);
           }
         }
       }
@@ -583,7 +583,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 #pragma unroll
               for (int t = 0; t < MT; ++t) {
                 const int c = V8 ? t : (t >> 1);
-                if (ONEG || ((VDC * c) >> A.v_group_shift) == g)
+                if ((VDC * c) / GS == g)
 #pragma unroll
                   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -626,7 +626,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         for (int cc = 0; cc < 2; ++cc) {
           const int c = 2 * c2 + cc;
           if constexpr (!ONEG) {
-            if (((VDC * c) & ((1 << A.v_group_shift) - 1)) == 0) weights((VDC * c) >> A.v_group_shift);
+            if ((VDC * c) % GS == 0) weights((VDC * c) / GS);
           }
           if constexpr (V8) {
             uint32_t h0[2], h8[2];
@@ -693,7 +693,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
           f = (t & 1) ? 1.0f / 16.0f : 1.0f;
         }
         const int c = V8 ? t : (t >> 1);
-        const int g = ONEG ? 0 : ((VDC * c) >> A.v_group_shift);
+        const int g = (VDC * c) / GS;
         float vi = vinv[0], pbg = pbs[0];
 #pragma unroll
         for (int gg = 1; gg < VNG; ++gg)
@@ -853,9 +853,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 }
 
 // Host launcher of one instantiation (dynamic shared memory, optional PDL).
-template <int KK, int VK, int HD, int NT, bool ONEG, int PT>
+template <int KK, int VK, int HD, int NT, int NG, int PT>
 kvq_status launch_tc_one(const TcArgs& t, dim3 grid, size_t smem, cudaStream_t stream, bool pdl) {
-  auto kern = decode_tc_kernel<KK, VK, HD, NT, ONEG, PT>;
+  auto kern = decode_tc_kernel<KK, VK, HD, NT, NG, PT>;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -880,29 +880,38 @@ kvq_status launch_tc_one(const TcArgs& t, dim3 grid, size_t smem, cudaStream_t s
 }
 
 // Shapes with a tensor-core instantiation: head_dim 64 and 256 with G <= 4,
-// head_dim 128 with any G.
-inline bool tc_has_shape(int head_dim, int nt) {
-  return head_dim == 128 || ((head_dim == 64 || head_dim == 256) && nt == 1);
+// head_dim 128 with any G; ng = head_dim / group scale groups per head, with
+// groups of at least 32 elements.
+inline bool tc_has_shape(int head_dim, int nt, int ng) {
+  const bool ng_ok = ng == 1 || ng == 2 || ng == 4 || ng == 8;
+  return ng_ok && head_dim / ng >= 32 && (head_dim == 128 || ((head_dim == 64 || head_dim == 256) && nt == 1));
 }
 
 template <int KK, int VK, int PT>
-kvq_status launch_tc_pt(const TcArgs& t, int head_dim, int nt, bool oneg, dim3 grid, size_t smem,
+kvq_status launch_tc_pt(const TcArgs& t, int head_dim, int nt, int ng, dim3 grid, size_t smem,
                         cudaStream_t stream, bool pdl) {
-#define KVQ_TC(HD_, NT_)                                                                           \
-  if (head_dim == HD_ && nt == NT_)                                                                \
-    return oneg ? launch_tc_one<KK, VK, HD_, NT_, true, PT>(t, grid, smem, stream, pdl)            \
-                : launch_tc_one<KK, VK, HD_, NT_, false, PT>(t, grid, smem, stream, pdl);
-  KVQ_TC(64, 1)
-  KVQ_TC(128, 1)
-  KVQ_TC(128, 2)
-  KVQ_TC(256, 1)
+#define KVQ_TC(HD_, NT_, NG_)                                          \
+  if (head_dim == HD_ && nt == NT_ && ng == NG_)                       \
+    return launch_tc_one<KK, VK, HD_, NT_, NG_, PT>(t, grid, smem, stream, pdl);
+  KVQ_TC(64, 1, 1)
+  KVQ_TC(64, 1, 2)
+  KVQ_TC(128, 1, 1)
+  KVQ_TC(128, 1, 2)
+  KVQ_TC(128, 1, 4)
+  KVQ_TC(128, 2, 1)
+  KVQ_TC(128, 2, 2)
+  KVQ_TC(128, 2, 4)
+  KVQ_TC(256, 1, 1)
+  KVQ_TC(256, 1, 2)
+  KVQ_TC(256, 1, 4)
+  KVQ_TC(256, 1, 8)
 #undef KVQ_TC
   return fail(KVQ_ERR_UNSUPPORTED, "no tensor-core decode kernel for head_dim %d", head_dim);
 }
 
 // One launcher per (K/V kind pair, scale type), each its own translation unit.
-typedef kvq_status (*TcLaunch)(const TcArgs&, int, int, bool, dim3, size_t, cudaStream_t, bool);
-#define KVQ_TC_DECLARE(NAME) kvq_status NAME(const TcArgs&, int, int, bool, dim3, size_t, cudaStream_t, bool);
+typedef kvq_status (*TcLaunch)(const TcArgs&, int, int, int, dim3, size_t, cudaStream_t, bool);
+#define KVQ_TC_DECLARE(NAME) kvq_status NAME(const TcArgs&, int, int, int, dim3, size_t, cudaStream_t, bool);
 KVQ_TC_DECLARE(launch_tc_s4s4_f32)
 KVQ_TC_DECLARE(launch_tc_s4s4_f16)
 KVQ_TC_DECLARE(launch_tc_s4s4_bf16)
