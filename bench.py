@@ -70,6 +70,35 @@ def algorithmic_bytes(w: dict, lens: np.ndarray, window: int) -> tuple[int, int]
     return dec, app
 
 
+KERNEL_SOURCES = ("int8_quantized_paged_gb300/csrc/kvq_decode_tc.cuh", "int8_quantized_paged_gb300/csrc/kvq_tc_ptx.cuh",
+                  "int8_quantized_paged_gb300/csrc/kvq_decode.cu")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes (read + write) of one decode launch of this workload from the
+    committed ncu summary (profiles/traffic.txt), or None when there is none or
+    the kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload:
+                    return int(parts[2]) if parts[1] == kernel_source_hash() else None
+    except OSError:
+        pass
+    return None
+
+
 def load_peaks() -> tuple[float, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -269,6 +298,43 @@ class BenchLayer:
             self.cache.decode(self.q, self.seq_lens, self.out, self.ws, self.chunk)
 
 
+def build_layers(args, dev, seed: int) -> list:
+    """The layers of args.workload's model, caches prefilled on the device."""
+    import torch
+    from int8_quantized_paged_gb300 import kvq
+    layers = []
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    rope_tabs = {}   # one RoPE table per model: every layer reads the same positions
+    for name, n, window in MODELS[args.workload]:
+        w = wl.workload(name, **({"batch": args.batch} if args.batch else {}))
+        if name not in rope_tabs:
+            cfg = kvq.config(**w)
+            rows = int(wl.seq_lens(w).max()) + 1
+            rope_tabs[name] = (torch.from_numpy(kvq.rope_table(cfg, rows)).to(dev)
+                               if cfg.rope != kvq.ROPE_NONE else None)
+        for i in range(n):
+            layers.append(BenchLayer(w, window, len(layers), dev, gen, args.chunk_tokens, rope_tabs[name]))
+    return layers
+
+
+def run_profile(args) -> None:
+    """Decode calls only, layer after layer, for profiler captures (no timing)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    from int8_quantized_paged_gb300 import build as _build
+    _build.build()
+    layers = build_layers(args, dev, 1000)
+    torch.cuda.synchronize()
+    for _ in range(args.profile_decode):
+        for L in layers:
+            L.decode()
+    torch.cuda.synchronize()
+    assert all(L.cache.status_bits() == 0 for L in layers), "a kernel flagged a bad input"
+    print(f"profile-decode: {args.workload}, {len(layers)} layers x {args.profile_decode} calls, "
+          f"{layers[0].dec_bytes} algorithmic bytes per call", flush=True)
+
+
 def run_gpu(args) -> dict | None:
     import torch
     rank, world, local = dist_env()
@@ -281,19 +347,7 @@ def run_gpu(args) -> dict | None:
     barrier(world)
     from int8_quantized_paged_gb300 import kvq
 
-    layers = []
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1000 + 97 * rank)
-    rope_tabs = {}   # one RoPE table per model: every layer reads the same positions
-    for name, n, window in MODELS[args.workload]:
-        w = wl.workload(name)
-        if name not in rope_tabs:
-            cfg = kvq.config(**w)
-            rows = int(wl.seq_lens(w).max()) + 1
-            rope_tabs[name] = (torch.from_numpy(kvq.rope_table(cfg, rows)).to(dev)
-                               if cfg.rope != kvq.ROPE_NONE else None)
-        for i in range(n):
-            layers.append(BenchLayer(w, window, len(layers), dev, gen, args.chunk_tokens, rope_tabs[name]))
+    layers = build_layers(args, dev, 1000 + 97 * rank)
     torch.cuda.synchronize()
     for L in layers:
         assert L.cache.status_bits() == 0, "prefill flagged a bad page or position"
@@ -326,7 +380,9 @@ def run_gpu(args) -> dict | None:
             cu.record_external(e0, torch.cuda.current_stream().cuda_stream)
             L.decode()
             cu.record_external(e1, torch.cuda.current_stream().cuda_stream)
-    launches_per_step = 3 * len(layers)   # append, split-K decode, combine
+    # per layer: the append kernel, plus the decode call's kernels (1 on the
+    # tensor-core path, 2 on the CUDA-core path)
+    launches_per_step = sum(1 + kvq.decode_launches(L.cache.cfg) for L in layers)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -402,7 +458,7 @@ def run_gpu(args) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int4/int8 codes, fp32 math",
+        "dtype": "int4/int8 codes; fp32 softmax and accumulation, fp16 hi/lo tensor-core operands",
         "data": "synthetic: seeded N(0,1) activations of the workload's shapes; no model weights",
         "config": {
             "workload": args.workload,
@@ -421,13 +477,13 @@ def run_gpu(args) -> dict | None:
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "roofline": {
             "bound": "hbm",
-            "kernel": "kvq_decode_attention (split-K decode + combine)",
+            "kernel": "decode_tc_kernel (kvq_decode_attention: split-K decode with the LSE combine fused)",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_source": f"{peak_kind} hbm_gbs",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": None,
+            "traffic": profiled_traffic(args.workload),
             "algorithmic_bytes_per_launch": int(dec_bytes),
             "avg_launch_us": round(dec_avg * 1e3, 3),
             "median_launch_us": round(statistics.median(dec_ms) * 1e3, 3),
@@ -556,8 +612,14 @@ def main():
     ap.add_argument("--chunk-tokens", type=int, default=0,
                     help="tokens per split-K chunk (0: the library chooses)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-decode", type=int, default=0, metavar="CALLS",
+                    help="only run CALLS decode calls per layer (for profiler captures)")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.profile_decode:
+        run_profile(args)
+        return
     if args.warmup < 3 and not args.cpu_worker and args.impl == "kvq":
         ap.error("--warmup must be >= 3")
 

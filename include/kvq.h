@@ -135,6 +135,12 @@ const char* kvq_last_error(void);
  * (INVALID_ARG / UNSUPPORTED) and a message. */
 kvq_status kvq_validate_config(const kvq_config* cfg);
 
+/* Kernel launches one kvq_decode_attention / kvq_window_decode call makes for
+ * cfg: 1 on the tensor-core path (split-K decode with the log-sum-exp combine
+ * fused in), 2 on the CUDA-core path (decode, then a combine kernel); 0 for an
+ * invalid config.  Not part of the method; it lets a caller count launches. */
+int32_t kvq_decode_launches(const kvq_config* cfg);
+
 /* ---------------------------------------------------------------- sizing --
  * Bytes of the K and V caches for n_layers layers holding ctx tokens each, with
  * ctx rounded up to whole pages.  This is the closed form 2 x layers x kv_heads

@@ -276,6 +276,12 @@ static kvq_status check_decode_args(const kvq_config* cfg, int32_t batch, const 
 
 using namespace kvq;
 
+extern "C" int32_t kvq_decode_launches(const kvq_config* cfg) {
+  clear_error();
+  if (check_kernel_config(cfg) != KVQ_OK) return 0;
+  return tc_enabled(*cfg) ? 1 : 2;
+}
+
 extern "C" size_t kvq_decode_workspace_bytes(const kvq_config* cfg, int32_t batch, int32_t max_pages_per_seq,
                                              int32_t chunk_tokens) {
   clear_error();

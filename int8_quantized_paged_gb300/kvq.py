@@ -61,6 +61,7 @@ _SIGS = {
     "kvq_abi_version": (_i32, []),
     "kvq_last_error": (C.c_char_p, []),
     "kvq_validate_config": (C.c_int, [_cfgp]),
+    "kvq_decode_launches": (_i32, [_cfgp]),
     "kvq_cache_bytes": (_sz, [_cfgp, _i32, _i64]),
     "kvq_page_bytes": (_sz, [_cfgp, _i32]),
     "kvq_pool_create": (C.c_int, [_i32, C.POINTER(_vp)]),
@@ -144,6 +145,14 @@ def abi_version() -> int:
 
 def validate_config(cfg: Config) -> None:
     _check(lib().kvq_validate_config(C.byref(cfg)))
+
+
+def decode_launches(cfg: Config) -> int:
+    """Kernel launches per decode call (1: tensor-core path, 2: CUDA-core path)."""
+    n = lib().kvq_decode_launches(C.byref(cfg))
+    if n == 0:
+        raise KvqError(ERR_INVALID_ARG, last_error())
+    return n
 
 
 def cache_bytes(cfg: Config, n_layers: int, ctx: int) -> int:
