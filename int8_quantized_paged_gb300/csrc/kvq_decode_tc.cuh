@@ -481,24 +481,16 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int c = 2 * c2 + cc;
+          // codes of tokens gid / gid+8 -> fp16 fragments -> MMAs, in one PTX block
           if constexpr (K8) {
-            uint32_t h0[2], h8[2];
-            tc::q8_codes(r[2 * cc], h0);
-            tc::q8_codes(r[2 * cc + 1], h8);
-            const uint32_t af[4] = {h0[0], h8[0], h0[1], h8[1]};
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) tc::mma_16816(sacc[nt], af, qb[nt][c][0], qb[nt][c][1]);
+            if constexpr (NT == 1) tc::qk8(r[2 * cc], r[2 * cc + 1], qb[0][c], sacc[0]);
+            else tc::qk8x2(r[2 * cc], r[2 * cc + 1], qb[0][c], qb[1][c], sacc[0], sacc[1]);
           } else {
-            uint32_t h0[4], h8[4];
-            tc::q4_codes<KAFF>(r[2 * cc], h0);
-            tc::q4_codes<KAFF>(r[2 * cc + 1], h8);
-            const uint32_t ae[4] = {h0[0], h8[0], h0[2], h8[2]};
-            const uint32_t ao[4] = {h0[1], h8[1], h0[3], h8[3]};
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              tc::mma_16816(sacc[nt], ae, qb[nt][2 * c][0], qb[nt][2 * c][1]);
-              tc::mma_16816(sacc[nt], ao, qb[nt][2 * c + 1][0], qb[nt][2 * c + 1][1]);
-            }
+            if constexpr (NT == 1)
+              tc::qk4<KAFF>(r[2 * cc], r[2 * cc + 1], qb[0][2 * c], qb[0][2 * c + 1], sacc[0]);
+            else
+              tc::qk4x2<KAFF>(r[2 * cc], r[2 * cc + 1], qb[0][2 * c], qb[0][2 * c + 1], qb[1][2 * c],
+                              qb[1][2 * c + 1], sacc[0], sacc[1]);
           }
           if constexpr (!ONEG) {
             if ((KDC * (c + 1)) % GS == 0) fold((KDC * c) / GS);
@@ -628,23 +620,16 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
           if constexpr (!ONEG) {
             if ((VDC * c) % GS == 0) weights((VDC * c) / GS);
           }
+          // V^T codes of chunk c -> fp16 fragments -> MMAs, in one PTX block
           if constexpr (V8) {
-            uint32_t h0[2], h8[2];
-            tc::q8_codes(y[2 * cc], h0);
-            tc::q8_codes(y[2 * cc + 1], h8);
-            const uint32_t af[4] = {h0[0], h0[1], h8[0], h8[1]};
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) tc::mma_16816(oacc[c][nt], af, bw[nt][0], bw[nt][1]);
+            for (int nt = 0; nt < NT; ++nt) tc::pv8(y[2 * cc], y[2 * cc + 1], bw[nt], oacc[c][nt]);
           } else {
-            uint32_t h0[4], h8[4];
-            tc::q4_codes<VAFF>(y[2 * cc], h0);
-            tc::q4_codes<VAFF>(y[2 * cc + 1], h8);
-#pragma unroll
-            for (int p2 = 0; p2 < 2; ++p2) {
-              const uint32_t af[4] = {h0[p2], h0[p2 + 2], h8[p2], h8[p2 + 2]};
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) tc::mma_16816(oacc[2 * c + p2][nt], af, bw[nt][0], bw[nt][1]);
-            }
+            if constexpr (NT == 1)
+              tc::pv4<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], oacc[2 * c][0], oacc[2 * c + 1][0]);
+            else
+              tc::pv4x2<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], bw[1], oacc[2 * c][0], oacc[2 * c + 1][0],
+                              oacc[2 * c][1], oacc[2 * c + 1][1]);
           }
         }
       }
