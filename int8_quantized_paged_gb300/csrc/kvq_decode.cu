@@ -206,7 +206,8 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     const int pt = cfg->k_param_dtype;
     if (t.kp_bytes != tc_scale_bytes(k, ng, pt) || t.vp_bytes != tc_scale_bytes(v, ng, pt))
       return fail(KVQ_ERR_UNSUPPORTED, "scale rows do not match the tensor-core kernel's slots");
-    size_t smem = (size_t)kWarps * tc_depth(cfg->head_dim, nt) * tc_slot_bytes(k, v, cfg->head_dim, ng, pt);
+    size_t smem = (size_t)kWarps * tc_depth(cfg->head_dim, nt) * tc_slot_bytes(k, v, cfg->head_dim, ng, pt) +
+                  tc_qfrag_bytes(cfg->head_dim, nt);
     const size_t need_merge = (size_t)kWarps * G * (cfg->head_dim + 2) * sizeof(float);
     // combine: (m, l) of every chunk, then the per-group column sums
     const size_t need_comb = (size_t)w.n_chunks * G * 2 * sizeof(float) + 16 +

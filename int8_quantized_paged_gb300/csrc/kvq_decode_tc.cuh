@@ -74,8 +74,11 @@ constexpr float kWScale = 128.0f;   // w is held x 2^7 (w <= 2^8 * 2^7 < 65504)
 constexpr float kLazyMax = 8.0f;    // raise the running max only past +2^8
 
 // Pages in flight per warp, and CTAs per SM (the launch bounds), by shape.
-__host__ __device__ constexpr int tc_depth(int hd, int nt) { return hd == 256 ? 3 : (nt == 2 ? 4 : 6); }
-__host__ __device__ constexpr int tc_min_blocks(int hd, int nt) { return (hd <= 128 && nt == 1) ? 4 : 3; }
+__host__ __device__ constexpr int tc_depth(int hd, int nt) { return hd == 256 ? 3 : 4; }
+__host__ __device__ constexpr int tc_min_blocks(int hd, int nt) { return (hd <= 128 && nt == 1) ? 5 : 3; }
+// Shared memory of the query fragments (the same for every warp of a CTA):
+// NT tiles x hd/16 k-steps x 2 words x 32 lanes.
+__host__ __device__ constexpr int tc_qfrag_bytes(int hd, int nt) { return nt * hd * 16; }
 
 // Shared-memory offset of 16-byte chunk `c` of row `r` in a block of rows of
 // ROWB bytes (32..256), with the chunk index XORed by a function of the row:
@@ -388,6 +391,22 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     }
   }
 
+  // The fragments are the same for every warp of the CTA: warp 0 keeps them in
+  // shared memory, [uint4 i][lane] with uint4 i = words of k-steps 2i, 2i+1,
+  // and every warp reloads the ones it needs per page (fewer live registers).
+  const uint32_t qfs = tc::smem_u32(smem) + (uint32_t)(NW * D * SLOT);
+  if (warp == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < KSTEPS / 2; ++i)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qfs + ((nt * (KSTEPS / 2) + i) * 32 + lane) * 16),
+                     "r"(qb[nt][2 * i][0]), "r"(qb[nt][2 * i][1]), "r"(qb[nt][2 * i + 1][0]),
+                     "r"(qb[nt][2 * i + 1][1])
+                     : "memory");
+  }
+  __syncthreads();
+
   // ---- per-lane constants of the main loop
   const int kprb = a.kl.param_row_bytes, vprb = a.vl.param_row_bytes;
   const int kstep = a.kl.n_params * PB, vstep = a.vl.n_params * PB;   // bytes per group in a param row
@@ -478,19 +497,37 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       for (int c2 = 0; c2 < KCH / 2; ++c2) {
         uint32_t r[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
         tc::ldsm_x4(kc + kls[c2], r);
+        // query fragments of chunks 2c2, 2c2+1: uint4s (K8: one for both, 4-bit: one each)
+        uint32_t qf[NT][2][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int cc = 0; cc < (K8 ? 1 : 2); ++cc) {
+            const int i = K8 ? c2 : 2 * c2 + cc;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(qf[nt][cc][0]), "=r"(qf[nt][cc][1]), "=r"(qf[nt][cc][2]), "=r"(qf[nt][cc][3])
+                         : "r"(qfs + ((nt * (KSTEPS / 2) + i) * 32 + lane) * 16));
+          }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int c = 2 * c2 + cc;
           // codes of tokens gid / gid+8 -> fp16 fragments -> MMAs, in one PTX block
-          if constexpr (K8) {
-            if constexpr (NT == 1) tc::qk8(r[2 * cc], r[2 * cc + 1], qb[0][c], sacc[0]);
-            else tc::qk8x2(r[2 * cc], r[2 * cc + 1], qb[0][c], qb[1][c], sacc[0], sacc[1]);
-          } else {
-            if constexpr (NT == 1)
-              tc::qk4<KAFF>(r[2 * cc], r[2 * cc + 1], qb[0][2 * c], qb[0][2 * c + 1], sacc[0]);
-            else
-              tc::qk4x2<KAFF>(r[2 * cc], r[2 * cc + 1], qb[0][2 * c], qb[0][2 * c + 1], qb[1][2 * c],
-                              qb[1][2 * c + 1], sacc[0], sacc[1]);
+          if constexpr (K8) {   // k-step c: words 2cc, 2cc+1 of the uint4
+            const uint32_t b0[2] = {qf[0][0][2 * cc], qf[0][0][2 * cc + 1]};
+            if constexpr (NT == 1) {
+              tc::qk8(r[2 * cc], r[2 * cc + 1], b0, sacc[0]);
+            } else {
+              const uint32_t b1[2] = {qf[1][0][2 * cc], qf[1][0][2 * cc + 1]};
+              tc::qk8x2(r[2 * cc], r[2 * cc + 1], b0, b1, sacc[0], sacc[1]);
+            }
+          } else {              // k-steps 2c, 2c+1: the uint4 of chunk c
+            const uint32_t be0[2] = {qf[0][cc][0], qf[0][cc][1]}, bo0[2] = {qf[0][cc][2], qf[0][cc][3]};
+            if constexpr (NT == 1) {
+              tc::qk4<KAFF>(r[2 * cc], r[2 * cc + 1], be0, bo0, sacc[0]);
+            } else {
+              const uint32_t be1[2] = {qf[1][cc][0], qf[1][cc][1]}, bo1[2] = {qf[1][cc][2], qf[1][cc][3]};
+              tc::qk4x2<KAFF>(r[2 * cc], r[2 * cc + 1], be0, bo0, be1, bo1, sacc[0], sacc[1]);
+            }
           }
           if constexpr (!ONEG) {
             if ((KDC * (c + 1)) % GS == 0) fold((KDC * c) / GS);
