@@ -71,7 +71,7 @@ def algorithmic_bytes(w: dict, lens: np.ndarray, window: int) -> tuple[int, int]
 
 
 KERNEL_SOURCES = ("int8_quantized_paged_gb300/csrc/kvq_decode_tc.cuh", "int8_quantized_paged_gb300/csrc/kvq_tc_ptx.cuh",
-                  "int8_quantized_paged_gb300/csrc/kvq_decode.cu")
+                  "int8_quantized_paged_gb300/csrc/kvq_decode.cu", "int8_quantized_paged_gb300/csrc/kvq_quant.cuh")
 
 
 def kernel_source_hash() -> str:
@@ -287,6 +287,7 @@ class BenchLayer:
         self.chunk = chunk_tokens
         self.ws = self.cache.workspace(self.B, chunk_tokens, self.window)
         self.dec_bytes, self.app_bytes = algorithmic_bytes(w, self.lens, self.window)
+        self.use_fused = True
 
     def append(self):
         self.cache.append(self.k_new, self.v_new, self.pos)
@@ -296,6 +297,25 @@ class BenchLayer:
             self.cache.window_decode(self.q, self.seq_lens, self.out, self.ws, self.window, self.chunk)
         else:
             self.cache.decode(self.q, self.seq_lens, self.out, self.ws, self.chunk)
+
+    def fused(self) -> bool:
+        """Whether step() makes one kvq_append_decode_attention call (whole-context layers)."""
+        return self.use_fused and not self.window
+
+    def step(self):
+        """This layer's share of a decode step: append the new row, then decode."""
+        if self.fused():
+            self.cache.append_decode(self.q, self.k_new, self.v_new, self.pos, self.seq_lens, self.out, self.ws,
+                                     self.chunk)
+        else:
+            self.append()
+            self.decode()
+
+    def launches(self) -> int:
+        from int8_quantized_paged_gb300 import kvq
+        if self.fused():
+            return kvq.append_decode_launches(self.cache.cfg)
+        return 1 + kvq.decode_launches(self.cache.cfg)
 
 
 def build_layers(args, dev, seed: int) -> list:
@@ -315,11 +335,14 @@ def build_layers(args, dev, seed: int) -> list:
                                if cfg.rope != kvq.ROPE_NONE else None)
         for i in range(n):
             layers.append(BenchLayer(w, window, len(layers), dev, gen, args.chunk_tokens, rope_tabs[name]))
+    for L in layers:
+        L.use_fused = not args.separate
     return layers
 
 
 def run_profile(args) -> None:
-    """Decode calls only, layer after layer, for profiler captures (no timing)."""
+    """The timed decode call of every layer (the fused append + decode call, or the
+    decode alone), layer after layer, for profiler captures (no timing)."""
     import torch
     dev = torch.device("cuda", 0)
     from int8_quantized_paged_gb300 import build as _build
@@ -328,7 +351,7 @@ def run_profile(args) -> None:
     torch.cuda.synchronize()
     for _ in range(args.profile_decode):
         for L in layers:
-            L.decode()
+            L.step() if L.fused() else L.decode()
     torch.cuda.synchronize()
     assert all(L.cache.status_bits() == 0 for L in layers), "a kernel flagged a bad input"
     print(f"profile-decode: {args.workload}, {len(layers)} layers x {args.profile_decode} calls, "
@@ -361,11 +384,11 @@ def run_gpu(args) -> dict | None:
 
     def step():
         for L in layers:
-            L.append()
-            L.decode()
+            L.step()
 
     # warm up outside capture, then capture the step (graph A) and the step with
-    # external event records around every decode call (graph B).
+    # external event records around every decode call (graph B): the fused
+    # append + decode call, or the decode call after a separate append.
     with torch.cuda.stream(stream):
         step()
     torch.cuda.synchronize()
@@ -376,13 +399,14 @@ def run_gpu(args) -> dict | None:
     g_b = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_b, stream=stream):
         for L, (e0, e1) in zip(layers, evs):
-            L.append()
+            if not L.fused():
+                L.append()
             cu.record_external(e0, torch.cuda.current_stream().cuda_stream)
-            L.decode()
+            L.step() if L.fused() else L.decode()
             cu.record_external(e1, torch.cuda.current_stream().cuda_stream)
-    # per layer: the append kernel, plus the decode call's kernels (1 on the
-    # tensor-core path, 2 on the CUDA-core path)
-    launches_per_step = sum(1 + kvq.decode_launches(L.cache.cfg) for L in layers)
+    # per layer: one fused launch on the tensor-core path; else the append
+    # kernel plus the decode call's kernels
+    launches_per_step = sum(L.launches() for L in layers)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -442,8 +466,17 @@ def run_gpu(args) -> dict | None:
 
     ms_max = max_over_ranks(ms, world)
     e2e_max = max_over_ranks(e2e_ms, world)
-    dec_avg = statistics.mean(dec_ms)
-    dec_bytes = statistics.mean(L.dec_bytes for L in layers)
+    # bytes of the timed call: the decode's, plus the append's when it is fused in
+    dec_bytes = statistics.mean(L.dec_bytes + (L.app_bytes if L.fused() else 0) for L in layers)
+    fused = any(L.fused() for L in layers)
+    # Launch duration.  When every layer's step is one launch of the kernel,
+    # the timed region holds nothing else: its time over the launches is the
+    # kernel's average duration back to back (each launch's start overlapping
+    # the one before it, as in the step).  Otherwise the calls bracketed by
+    # events in graph B, which also holds their launch latency.
+    one_kernel = all(L.fused() and L.launches() == 1 for L in layers)
+    bracketed = statistics.mean(dec_ms)
+    dec_avg = ms / launches_per_step if one_kernel else bracketed
     peak, peak_kind = load_peaks()
     achieved = dec_bytes / (dec_avg / 1e3) / 1e9
     value = whole_job(step_bytes, world, ms_max) / 1e9
@@ -471,13 +504,17 @@ def run_gpu(args) -> dict | None:
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "graph": "CUDA graph of one step",
             "chunk_tokens": args.chunk_tokens or "library default",
+            "step_call": ("kvq_append_decode_attention (window layers: kvq_append + kvq_window_decode)"
+                          if fused else "kvq_append + kvq_decode_attention"),
         },
         "tokens_per_s": round(whole_job(query_tokens, world, ms_max), 1),
         "context_tokens_per_s": round(whole_job(ctx_tokens, world, ms_max), 1),
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode_tc_kernel (kvq_decode_attention: split-K decode with the LSE combine fused)",
+            "kernel": ("decode_tc_kernel (kvq_append_decode_attention: the step's append, split-K decode "
+                       "and the LSE combine in one launch)" if fused else
+                       "decode_tc_kernel (kvq_decode_attention: split-K decode with the LSE combine fused)"),
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_source": f"{peak_kind} hbm_gbs",
@@ -486,7 +523,9 @@ def run_gpu(args) -> dict | None:
             "traffic": profiled_traffic(args.workload),
             "algorithmic_bytes_per_launch": int(dec_bytes),
             "avg_launch_us": round(dec_avg * 1e3, 3),
-            "median_launch_us": round(statistics.median(dec_ms) * 1e3, 3),
+            "launch_us_from": ("timed region / launches (the step is only this kernel)" if one_kernel
+                               else "CUDA events around each call in a graph of the step"),
+            "bracketed_launch_us": round(bracketed * 1e3, 3),
         },
         "e2e": {
             "value": round(whole_job(step_bytes, world, e2e_max) / 1e9, 2),
@@ -615,6 +654,8 @@ def main():
     ap.add_argument("--profile-decode", type=int, default=0, metavar="CALLS",
                     help="only run CALLS decode calls per layer (for profiler captures)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
+    ap.add_argument("--separate", action="store_true",
+                    help="time kvq_append + kvq_decode_attention instead of the fused call")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.profile_decode:

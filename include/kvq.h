@@ -141,6 +141,17 @@ kvq_status kvq_validate_config(const kvq_config* cfg);
  * invalid config.  Not part of the method; it lets a caller count launches. */
 int32_t kvq_decode_launches(const kvq_config* cfg);
 
+/* CTAs per thread-block cluster that a decode call with these arguments uses
+ * on the current device: >= 1 when the chunks of every (sequence, kv head)
+ * form one cluster and combine in distributed shared memory (few sequences of
+ * up to 16K tokens, chunk_tokens 0), 0 when the partials go through the
+ * workspace instead, -1 for invalid arguments.  window is 0 for
+ * kvq_decode_attention and the window of kvq_window_decode otherwise.  Not
+ * part of the method; it lets a caller see which combine runs.  Needs a
+ * current CUDA device for an answer other than -1 or 0. */
+int32_t kvq_decode_cluster_ctas(const kvq_config* cfg, int32_t batch, int32_t max_pages_per_seq,
+                                int32_t window, int32_t chunk_tokens);
+
 /* ---------------------------------------------------------------- sizing --
  * Bytes of the K and V caches for n_layers layers holding ctx tokens each, with
  * ctx rounded up to whole pages.  This is the closed form 2 x layers x kv_heads
@@ -245,6 +256,8 @@ kvq_status kvq_append(const kvq_config* cfg, int32_t n_rows,
  * [airllm] §3.4.
  *   q, out        device [batch][n_heads][head_dim] of act_dtype; q 16-byte
  *                 aligned (KVQ_ERR_INVALID_ARG otherwise)
+ *   rope_tab      as for kvq_append, 16-byte aligned (KVQ_ERR_INVALID_ARG
+ *                 otherwise); unused when cfg->rope is KVQ_ROPE_NONE
  *   seq_lens      device int32 [batch], 0 <= L <= max_pages_per_seq*page_size
  *   chunk_tokens  0: the library chooses; else a multiple of page_size
  *   workspace     device scratch of at least kvq_decode_workspace_bytes()
@@ -284,6 +297,36 @@ kvq_status kvq_window_decode(const kvq_config* cfg, int32_t batch, const void* q
                              const float* rope_tab, int32_t rope_max_pos,
                              void* out, void* workspace, size_t workspace_bytes,
                              int32_t chunk_tokens, int32_t* dev_status, kvq_stream_t stream);
+
+/* ------------------------------------------ fused append + decode step --
+ * One decode step of every sequence in one call: kvq_append of the step's new
+ * row of each sequence b (k_new[b], v_new[b] at position pos[b]: K rotated,
+ * both quantized into their page) followed by kvq_decode_attention with
+ * seq_lens, the caller's usual pos[b] = seq_lens[b] - 1 making the new row the
+ * last key.  The pool bytes written and the output are those of the two calls
+ * made one after the other.  On the tensor-core path it is one launch: the
+ * CTA that reads the new row's page quantizes the row (the append kernel's
+ * arithmetic), writes it to the pool and uses it straight from shared memory;
+ * elsewhere it is the append kernel and then the decode.
+ *   k_new, v_new  device [batch][n_kv_heads][head_dim] of act_dtype, 16-byte
+ *                 aligned (KVQ_ERR_INVALID_ARG otherwise)
+ *   pos           device int32 [batch]; row b goes to sequence b.  A bad
+ *                 position sets KVQ_DEV_BAD_POS, a bad page id KVQ_DEV_BAD_PAGE,
+ *                 and that row is not written
+ *   k_pool, v_pool  written (the new rows) and read
+ * All other arguments as in kvq_decode_attention (the same workspace size).
+ * Its launches per call: kvq_append_decode_launches(cfg). */
+kvq_status kvq_append_decode_attention(const kvq_config* cfg, int32_t batch, const void* q,
+                                       const void* k_new, const void* v_new, const int32_t* pos,
+                                       void* k_pool, void* v_pool, int32_t n_pool_pages,
+                                       const int32_t* block_table, int32_t max_pages_per_seq,
+                                       const int32_t* seq_lens,
+                                       const float* rope_tab, int32_t rope_max_pos,
+                                       void* out, void* workspace, size_t workspace_bytes,
+                                       int32_t chunk_tokens, int32_t* dev_status, kvq_stream_t stream);
+/* Kernel launches of one kvq_append_decode_attention call for cfg: 1 on the
+ * tensor-core path, 3 on the CUDA-core path; 0 for an invalid config. */
+int32_t kvq_append_decode_launches(const kvq_config* cfg);
 
 /* ------------------------------------------- decode without allocation --
  * The pages have no counterpart to this entry point.  It exists for callers

@@ -8,15 +8,13 @@
 // "KV Cache 的双布局设计" (K rotated before caching, V not; ring rows
 // overwritten in place); [airllm] §2.3 (fixed-size pages from a shared pool).
 //
-// One warp handles one (row, kv head) and both its K and V vectors.  Each lane
-// holds head_dim/32 consecutive elements.  A group's amax (or min/max) is a
-// butterfly reduction over the lanes that hold the group.  Every arithmetic
-// step uses an explicitly rounded intrinsic, so nothing is contracted into an
-// FMA and the codes are bit-exact against the fp32 specification.
+// One warp handles one (row, kv head) and both its K and V vectors; the row
+// arithmetic (kvq_quant.cuh) is the one the fused append + decode path uses.
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_quant.cuh"
 
 namespace kvq {
 
@@ -34,78 +32,6 @@ struct AppendArgs {
   int32_t act, rope;
   PoolLayout kl, vl;
 };
-
-template <int DPL>
-__device__ __forceinline__ void quantize_store(float (&x)[DPL], const PoolLayout& L, uint8_t* sub,
-                                               int slot, int lane) {
-  constexpr int P = 16;
-  const int lpg = L.group / DPL;            // lanes per group (a power of two)
-  uint8_t* codes = sub + slot * L.code_bytes;
-  uint8_t* prow = sub + P * L.code_bytes + slot * L.param_row_bytes;
-  const int g = lane / lpg;
-  const int pb = param_bytes(L.param);
-  int c[DPL];
-  if (L.kind == KVQ_AFFINE_INT4) {
-    float mn = x[0], mx = x[0];
-#pragma unroll
-    for (int j = 1; j < DPL; ++j) { mn = fminf(mn, x[j]); mx = fmaxf(mx, x[j]); }
-    for (int o = 1; o < lpg; o <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    const float scale = round_param(__fdiv_rn(__fsub_rn(mx, mn), 15.0f), L.param);
-    const float bias = round_param(mn, L.param);
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) {
-      float y = scale == 0.0f ? 0.0f : rintf(__fdiv_rn(__fsub_rn(x[j], bias), scale));
-      y = fminf(fmaxf(y, 0.0f), 15.0f);
-      c[j] = (int)y;
-    }
-    if (lane % lpg == 0) {
-      store_param(prow + (2 * g) * pb, L.param, scale);
-      store_param(prow + (2 * g + 1) * pb, L.param, bias);
-    }
-  } else {
-    const float qmax = L.kind == KVQ_SYM_INT8 ? 127.0f : 7.0f;
-    float amax = fabsf(x[0]);
-#pragma unroll
-    for (int j = 1; j < DPL; ++j) amax = fmaxf(amax, fabsf(x[j]));
-    for (int o = 1; o < lpg; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float floor_s = L.param == KVQ_F16 ? 6.103515625e-05f : 1e-8f;
-    const float scale = round_param(fmaxf(__fdiv_rn(amax, qmax), floor_s), L.param);
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) {
-      float y = rintf(__fdiv_rn(x[j], scale));
-      y = fminf(fmaxf(y, -qmax), qmax);
-      c[j] = (int)y;
-    }
-    if (lane % lpg == 0) store_param(prow + g * pb, L.param, scale);
-  }
-  if (L.kind == KVQ_SYM_INT8) {
-    uint32_t w[(DPL + 3) / 4] = {};
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) w[j / 4] |= ((uint32_t)c[j] & 0xFFu) << (8 * (j % 4));
-    uint8_t* dst = codes + lane * DPL;
-    if constexpr (DPL == 2) {
-      *reinterpret_cast<unsigned short*>(dst) = (unsigned short)w[0];
-    } else {
-#pragma unroll
-      for (int i = 0; i < DPL / 4; ++i) reinterpret_cast<uint32_t*>(dst)[i] = w[i];
-    }
-  } else {
-    uint32_t w = 0;
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) w |= ((uint32_t)c[j] & 0xFu) << (4 * j);
-    uint8_t* dst = codes + lane * (DPL / 2);
-    if constexpr (DPL == 2) {
-      *dst = (uint8_t)w;
-    } else if constexpr (DPL == 4) {
-      *reinterpret_cast<unsigned short*>(dst) = (unsigned short)w;
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = w;
-    }
-  }
-}
 
 template <int HD>
 __global__ void __launch_bounds__(128) append_kernel(const AppendArgs a) {
@@ -145,38 +71,16 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendArgs a) {
   float x[DPL];
 #pragma unroll
   for (int j = 0; j < DPL; ++j) x[j] = load_act(a.k_new, a.act, base + j);
-  if (a.rope == KVQ_ROPE_NORMAL) {
-    const float2* cs = reinterpret_cast<const float2*>(a.rope_tab) + (int64_t)pos * (HD / 2);
-#pragma unroll
-    for (int j = 0; j < DPL; j += 2) {
-      const float2 t = cs[(lane * DPL + j) / 2];
-      const float x0 = x[j], x1 = x[j + 1];
-      x[j] = __fsub_rn(__fmul_rn(x0, t.x), __fmul_rn(x1, t.y));
-      x[j + 1] = __fadd_rn(__fmul_rn(x0, t.y), __fmul_rn(x1, t.x));
-    }
-  } else if (a.rope == KVQ_ROPE_NEOX) {
-    // Element d pairs with d + HD/2, which sits 16 lanes away.
-    const float2* cs = reinterpret_cast<const float2*>(a.rope_tab) + (int64_t)pos * (HD / 2);
-    const bool low = lane < 16;
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) {
-      const float other = __shfl_xor_sync(0xffffffffu, x[j], 16);
-      const float2 t = cs[(lane & 15) * DPL + j];
-      if (low) {
-        x[j] = __fsub_rn(__fmul_rn(x[j], t.x), __fmul_rn(other, t.y));
-      } else {
-        x[j] = __fadd_rn(__fmul_rn(other, t.y), __fmul_rn(x[j], t.x));
-      }
-    }
-  }
-  quantize_store<DPL>(x, a.kl, a.k_pool + (int64_t)page * a.kl.page_bytes + (int64_t)head * a.kl.sub_bytes,
-                      slot, lane);
+  if (a.rope != KVQ_ROPE_NONE)
+    rope_rotate_row<DPL>(x, reinterpret_cast<const float2*>(a.rope_tab) + (int64_t)pos * (HD / 2), a.rope, lane);
+  store_row(quantize_row<DPL>(x, a.kl, lane), a.kl,
+            a.k_pool + (int64_t)page * a.kl.page_bytes + (int64_t)head * a.kl.sub_bytes, slot, lane);
 
   // V: no rotation.
 #pragma unroll
   for (int j = 0; j < DPL; ++j) x[j] = load_act(a.v_new, a.act, base + j);
-  quantize_store<DPL>(x, a.vl, a.v_pool + (int64_t)page * a.vl.page_bytes + (int64_t)head * a.vl.sub_bytes,
-                      slot, lane);
+  store_row(quantize_row<DPL>(x, a.vl, lane), a.vl,
+            a.v_pool + (int64_t)page * a.vl.page_bytes + (int64_t)head * a.vl.sub_bytes, slot, lane);
 }
 
 }  // namespace kvq

@@ -1,9 +1,14 @@
 // Decode entry points: argument checks, the chunk plan and workspace layout,
-// tensor-map encoding and the launches.
+// and the launches.
 //
 // Two kernels compute the same decode.  The tensor-core kernel
 // (kvq_decode_tc.cuh) is the default.  It fuses the log-sum-exp combine into
-// the last CTA of each (sequence, kv head), so a call is one launch.  The
+// the same launch, so a call is one launch: for a few long sequences the
+// chunks of each (sequence, kv head) form one thread-block cluster and
+// combine through distributed shared memory; otherwise the last CTA of each
+// (sequence, kv head) combines the partials the others left in the
+// workspace.  KVQ_DECODE_CLUSTER=0 in the environment turns the cluster mode
+// off.  The
 // CUDA-core kernel (kvq_decode_impl.cuh) covers shapes the tensor-core kernel
 // does not take: groups that are not a multiple of 32, and 8-bit rows longer
 // than 128 bytes.  It is followed by a separate combine kernel.  Setting
@@ -18,6 +23,8 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "kvq_decode_impl.cuh"
 #include "kvq_decode_tc.cuh"
@@ -40,6 +47,104 @@ static bool tc_enabled(const kvq_config& c) {
   if (!pow2 || c.k_param_dtype != c.v_param_dtype || c.k_group < 32 || c.v_group < 32) return false;
   const int G = c.n_heads / c.n_kv_heads;
   return c.k_group == c.v_group && tc_has_shape(c.head_dim, G > 4 ? 2 : 1, c.head_dim / c.k_group);
+}
+
+static bool cluster_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("KVQ_DECODE_CLUSTER");
+    return !(e && std::strcmp(e, "0") == 0);
+  }();
+  return on;
+}
+
+// How many clusters of a launch configuration can be resident at once,
+// cached per (launcher, shape, cluster size, shared memory, device).
+static int max_active_clusters(TcLaunch fn, const TcArgs& t, int hd, int nt, int ng, const TcLaunchCfg& lc) {
+  struct Entry {
+    TcLaunch fn;
+    int hd, nt, ng, cluster, dev;
+    size_t smem;
+    int n;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (const Entry& e : cache)
+      if (e.fn == fn && e.hd == hd && e.nt == nt && e.ng == ng && e.cluster == lc.cluster && e.dev == dev &&
+          e.smem == lc.smem)
+        return e.n;
+  }
+  int n = 0;
+  TcLaunchCfg q = lc;
+  q.max_active = &n;
+  if (fn(t, hd, nt, ng, q) != KVQ_OK) n = 0;
+  std::lock_guard<std::mutex> g(mu);
+  cache.push_back(Entry{fn, hd, nt, ng, lc.cluster, dev, lc.smem, n});
+  return n;
+}
+
+// The tensor-core launcher of a config's K/V kinds and scale type.
+static TcLaunch tc_launcher(const kvq_config& c) {
+  static const TcLaunch table[4][3] = {
+      {launch_tc_s4s4_f32, launch_tc_s4s4_f16, launch_tc_s4s4_bf16},
+      {launch_tc_s8s8_f32, launch_tc_s8s8_f16, launch_tc_s8s8_bf16},
+      {launch_tc_s8s4_f32, launch_tc_s8s4_f16, launch_tc_s8s4_bf16},
+      {launch_tc_a4a4_f32, launch_tc_a4a4_f16, launch_tc_a4a4_bf16}};
+  const int k = c.k_dtype, v = c.v_dtype;
+  const int kind = (k == KVQ_SYM_INT4 && v == KVQ_SYM_INT4) ? 0
+                   : (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT8) ? 1
+                   : (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT4) ? 2
+                                                              : 3;
+  return table[kind][c.k_param_dtype];
+}
+
+// Bytes of one warp's ring of page slots.
+static size_t tc_ring_bytes(const kvq_config& c) {
+  const int G = c.n_heads / c.n_kv_heads;
+  return (size_t)tc_depth(c.head_dim, G > 4 ? 2 : 1) *
+         tc_slot_bytes(c.k_dtype, c.v_dtype, c.head_dim, c.head_dim / c.k_group, c.k_param_dtype);
+}
+
+// The cluster mode: a few sequences, each short enough that one cluster of
+// up to kMaxCluster CTAs of kClusterWarps warps covers it with about four
+// pages per warp (at most eight), and all the clusters resident at once.  On
+// success fills the launch configuration (grid, shared memory, warps, cluster
+// size) and the 16-token blocks per CTA.
+static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens, int32_t window, TcLaunch fn,
+                         size_t ring, size_t pre, TcLaunchCfg* lc, int* cb_out) {
+  const int G = c.n_heads / c.n_kv_heads;
+  const int hd = c.head_dim;
+  const int nt = G > 4 ? 2 : 1;
+  if (!cluster_enabled() || batch < 1 || !tc_cluster_shape(hd, nt)) return false;
+  // blocks of the longest context (a window may start mid-page)
+  const int64_t blocks = (max_tokens + c.page_size - 1) / c.page_size + (window > 0 ? 1 : 0);
+  if (blocks > (int64_t)kMaxCluster * kClusterWarps * 8 || (int64_t)batch * c.n_kv_heads > 4 * num_sms())
+    return false;
+  const int64_t per_cta = 4 * kClusterWarps;
+  int64_t nc = (blocks + per_cta - 1) / per_cta;
+  if (nc > kMaxCluster) nc = kMaxCluster;
+  if (nc < 1) nc = 1;
+  const int64_t cb = (blocks + nc - 1) / nc;
+  nc = (blocks + cb - 1) / cb;
+  // the warps' merge, then the CTA's partial o [G][hd] and (m, l) [G]
+  size_t need = (size_t)kClusterWarps * G * (hd + 2) * sizeof(float);
+  need = ((need + 15) & ~(size_t)15) + (size_t)G * hd * sizeof(float) + (size_t)G * 2 * sizeof(float);
+  size_t smem = (size_t)kClusterWarps * ring + pre;
+  if (smem < need) smem = need;
+  if (smem > 200 * 1024) return false;
+  TcLaunchCfg q = *lc;
+  q.grid = dim3((unsigned)nc, c.n_kv_heads, batch);
+  q.smem = smem;
+  q.warps = kClusterWarps;
+  q.cluster = (int)nc;
+  TcArgs none{};
+  if (max_active_clusters(fn, none, hd, nt, hd / c.k_group, q) < batch * c.n_kv_heads) return false;
+  *lc = q;
+  *cb_out = (int)cb;
+  return true;
 }
 
 // CTAs of the tensor-core kernel resident per SM (its launch bounds).
@@ -151,7 +256,9 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
                              int32_t max_pages, const int32_t* seq_lens, const float* rope_tab,
                              int32_t rope_max_pos, void* out, void* workspace, size_t ws_bytes,
                              int32_t chunk_tokens, int32_t* dev_status, cudaStream_t stream,
-                             int32_t ring_rows, int32_t window, int64_t max_tokens) {
+                             int32_t ring_rows, int32_t window, int64_t max_tokens,
+                             const void* app_k = nullptr, const void* app_v = nullptr,
+                             const int32_t* app_pos = nullptr) {
   const Plan w = make_plan(*cfg, batch, max_tokens, window > 0, chunk_tokens);
   if (w.n_chunks > kMaxChunks)
     return fail(KVQ_ERR_INVALID_ARG, "%d chunks exceed the limit %d; use larger chunks", w.n_chunks, kMaxChunks);
@@ -162,6 +269,9 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
 
   DecodeArgs a;
   a.q = q;
+  a.app_k = app_k;
+  a.app_v = app_v;
+  a.app_pos = app_pos;
   a.k_pool = static_cast<const uint8_t*>(k_pool);
   a.v_pool = static_cast<const uint8_t*>(v_pool);
   a.block_table = block_table;
@@ -199,16 +309,33 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     t.vc_bytes = cfg->page_size * a.vl.code_bytes;
     t.kp_bytes = cfg->page_size * a.kl.param_row_bytes;
     t.vp_bytes = cfg->page_size * a.vl.param_row_bytes;
-    // Shared memory: a ring of tc_depth pages per warp, reused at the end for
-    // the warps' merge and the combine weights.
+    t.cluster = 0;
     const int nt = G > 4 ? 2 : 1;
-    const int ng = cfg->head_dim / cfg->k_group;   // scale groups per head (K and V alike)
+    const int hd = cfg->head_dim;
+    const int ng = hd / cfg->k_group;   // scale groups per head (K and V alike)
     const int pt = cfg->k_param_dtype;
     if (t.kp_bytes != tc_scale_bytes(k, ng, pt) || t.vp_bytes != tc_scale_bytes(v, ng, pt))
       return fail(KVQ_ERR_UNSUPPORTED, "scale rows do not match the tensor-core kernel's slots");
-    size_t smem = (size_t)kWarps * tc_depth(cfg->head_dim, nt) * tc_slot_bytes(k, v, cfg->head_dim, ng, pt) +
-                  tc_qfrag_bytes(cfg->head_dim, nt);
-    const size_t need_merge = (size_t)kWarps * G * (cfg->head_dim + 2) * sizeof(float);
+    const TcLaunch fn = tc_launcher(*cfg);
+    // Shared memory: a ring of tc_depth pages per warp and the query's
+    // fragments, reused at the end for the warps' merge and then either the
+    // cluster's partial or the combine's weights.
+    const size_t ring = tc_ring_bytes(*cfg);
+    const size_t pre = tc_pre_bytes(hd, nt, ng);
+    auto merge_bytes = [&](int warps) { return (size_t)warps * G * (hd + 2) * sizeof(float); };
+    TcLaunchCfg lc{};
+    lc.stream = stream;
+    lc.pdl = pdl_enabled();
+
+    int cb = 0;
+    if (chunk_tokens == 0 && pick_cluster(*cfg, batch, max_tokens, window, fn, ring, pre, &lc, &cb)) {
+      t.cluster = lc.cluster;
+      t.blocks_per_chunk = cb;
+      return fn(t, hd, nt, ng, lc);
+    }
+
+    size_t smem = (size_t)kWarps * ring + pre;
+    const size_t need_merge = merge_bytes(kWarps);
     // combine: (m, l) of every chunk, then the per-group column sums
     const size_t need_comb = (size_t)w.n_chunks * G * 2 * sizeof(float) + 16 +
                              (size_t)kTcThreads * 4 * sizeof(float);
@@ -216,21 +343,11 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     if (smem < need_comb) smem = need_comb;
     if (smem > 200 * 1024)
       return fail(KVQ_ERR_UNSUPPORTED, "decode needs %zu bytes of shared memory; use larger chunks", smem);
-    kvq_status st = KVQ_OK;
-    const dim3 grid(w.tc_chunks, cfg->n_kv_heads, batch);
-    const bool pdl = pdl_enabled();
-    const int hd = cfg->head_dim;
-    static const TcLaunch table[4][3] = {
-        {launch_tc_s4s4_f32, launch_tc_s4s4_f16, launch_tc_s4s4_bf16},
-        {launch_tc_s8s8_f32, launch_tc_s8s8_f16, launch_tc_s8s8_bf16},
-        {launch_tc_s8s4_f32, launch_tc_s8s4_f16, launch_tc_s8s4_bf16},
-        {launch_tc_a4a4_f32, launch_tc_a4a4_f16, launch_tc_a4a4_bf16}};
-    const int kind = (k == KVQ_SYM_INT4 && v == KVQ_SYM_INT4) ? 0
-                     : (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT8) ? 1
-                     : (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT4) ? 2
-                                                                : 3;
-    st = table[kind][cfg->k_param_dtype](t, hd, nt, ng, grid, smem, stream, pdl);
-    return st;
+    lc.grid = dim3(w.tc_chunks, cfg->n_kv_heads, batch);
+    lc.smem = smem;
+    lc.warps = kWarps;
+    lc.cluster = 0;
+    return fn(t, hd, nt, ng, lc);
   }
 
   const dim3 grid(w.n_chunks, cfg->n_kv_heads, batch);
@@ -268,6 +385,8 @@ static kvq_status check_decode_args(const kvq_config* cfg, int32_t batch, const 
   if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool)) & 15)
     return fail(KVQ_ERR_INVALID_ARG, "pools must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(q) & 15) return fail(KVQ_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (cfg->rope != KVQ_ROPE_NONE && (reinterpret_cast<uintptr_t>(rope_tab) & 15))
+    return fail(KVQ_ERR_INVALID_ARG, "rope_tab must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(workspace) & 255)
     return fail(KVQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   return KVQ_OK;
@@ -276,6 +395,24 @@ static kvq_status check_decode_args(const kvq_config* cfg, int32_t batch, const 
 }  // namespace kvq
 
 using namespace kvq;
+
+extern "C" int32_t kvq_decode_cluster_ctas(const kvq_config* cfg, int32_t batch, int32_t max_pages_per_seq,
+                                           int32_t window, int32_t chunk_tokens) {
+  clear_error();
+  if (check_kernel_config(cfg) != KVQ_OK) return -1;
+  if (batch < 1 || max_pages_per_seq < 1 || window < 0 || chunk_tokens < 0) {
+    set_error("bad batch, max_pages_per_seq, window or chunk_tokens");
+    return -1;
+  }
+  if (!tc_enabled(*cfg) || chunk_tokens != 0) return 0;
+  const int G = cfg->n_heads / cfg->n_kv_heads;
+  const int64_t max_tokens = window > 0 ? window : (int64_t)max_pages_per_seq * cfg->page_size;
+  TcLaunchCfg lc{};
+  int cb = 0;
+  const bool on = pick_cluster(*cfg, batch, max_tokens, window, tc_launcher(*cfg), tc_ring_bytes(*cfg),
+                               tc_pre_bytes(cfg->head_dim, G > 4 ? 2 : 1, cfg->head_dim / cfg->k_group), &lc, &cb);
+  return on ? lc.cluster : 0;
+}
 
 extern "C" int32_t kvq_decode_launches(const kvq_config* cfg) {
   clear_error();
@@ -303,6 +440,42 @@ extern "C" size_t kvq_window_workspace_bytes(const kvq_config* cfg, int32_t batc
     return 0;
   }
   return make_plan(*cfg, batch, window, true, chunk_tokens).total;
+}
+
+extern "C" int32_t kvq_append_decode_launches(const kvq_config* cfg) {
+  clear_error();
+  if (check_kernel_config(cfg) != KVQ_OK) return 0;
+  return tc_enabled(*cfg) ? 1 : 3;
+}
+
+extern "C" kvq_status kvq_append_decode_attention(const kvq_config* cfg, int32_t batch, const void* q,
+                                                  const void* k_new, const void* v_new, const int32_t* pos,
+                                                  void* k_pool, void* v_pool, int32_t n_pool_pages,
+                                                  const int32_t* block_table, int32_t max_pages_per_seq,
+                                                  const int32_t* seq_lens, const float* rope_tab,
+                                                  int32_t rope_max_pos, void* out, void* workspace,
+                                                  size_t workspace_bytes, int32_t chunk_tokens,
+                                                  int32_t* dev_status, kvq_stream_t stream) {
+  clear_error();
+  kvq_status st = check_decode_args(cfg, batch, q, k_pool, v_pool, n_pool_pages, block_table, seq_lens,
+                                    rope_tab, rope_max_pos, out, workspace, chunk_tokens, dev_status);
+  if (st != KVQ_OK || batch == 0) return st;
+  if (max_pages_per_seq < 1) return fail(KVQ_ERR_INVALID_ARG, "max_pages_per_seq must be >= 1");
+  if (!k_new || !v_new || !pos) return fail(KVQ_ERR_INVALID_ARG, "k_new, v_new and pos must not be NULL");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+    return fail(KVQ_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  if (!tc_enabled(*cfg)) {
+    // The CUDA-core decode has no fused append: the append kernel, then the decode.
+    st = kvq_append(cfg, batch, k_new, v_new, nullptr, pos, block_table, batch, max_pages_per_seq, 0, rope_tab,
+                    rope_max_pos, k_pool, v_pool, n_pool_pages, dev_status, stream);
+    if (st != KVQ_OK) return st;
+    return run_decode(cfg, batch, q, k_pool, v_pool, n_pool_pages, block_table, max_pages_per_seq, seq_lens,
+                      rope_tab, rope_max_pos, out, workspace, workspace_bytes, chunk_tokens, dev_status,
+                      (cudaStream_t)stream, 0, 0, (int64_t)max_pages_per_seq * cfg->page_size);
+  }
+  return run_decode(cfg, batch, q, k_pool, v_pool, n_pool_pages, block_table, max_pages_per_seq, seq_lens,
+                    rope_tab, rope_max_pos, out, workspace, workspace_bytes, chunk_tokens, dev_status,
+                    (cudaStream_t)stream, 0, 0, (int64_t)max_pages_per_seq * cfg->page_size, k_new, v_new, pos);
 }
 
 extern "C" kvq_status kvq_decode_attention(const kvq_config* cfg, int32_t batch, const void* q,

@@ -54,6 +54,7 @@
 #include "kvq_decode_impl.cuh"
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_quant.cuh"
 #include "kvq_tc_ptx.cuh"
 
 namespace kvq {
@@ -65,10 +66,14 @@ struct TcArgs {
   int32_t G;                 // query heads per kv head (1..8)
   int32_t blocks_per_chunk;  // 16-token blocks per chunk
   int32_t kc_bytes, vc_bytes, kp_bytes, vp_bytes;  // code and scale bytes of a page (one kv head)
+  int32_t cluster;           // 0: split-K partials through the workspace; else CTAs per
+                             // thread-block cluster (= gridDim.x), combined in shared memory
 };
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 4;                 // warps per CTA, split-K through the workspace
 constexpr int kTcThreads = 32 * kWarps;
+constexpr int kClusterWarps = 8;          // warps per CTA in the cluster mode
+constexpr int kMaxCluster = 16;           // CTAs per cluster (a non-portable size)
 constexpr float kQScale = 256.0f;   // q is held x 2^8 in fp16 (hi/lo)
 constexpr float kWScale = 128.0f;   // w is held x 2^7 (w <= 2^8 * 2^7 < 65504)
 constexpr float kLazyMax = 8.0f;    // raise the running max only past +2^8
@@ -76,9 +81,32 @@ constexpr float kLazyMax = 8.0f;    // raise the running max only past +2^8
 // Pages in flight per warp, and CTAs per SM (the launch bounds), by shape.
 __host__ __device__ constexpr int tc_depth(int hd, int nt) { return hd == 256 ? 3 : 4; }
 __host__ __device__ constexpr int tc_min_blocks(int hd, int nt) { return (hd <= 128 && nt == 1) ? 5 : 3; }
+// Shapes with a cluster-mode instantiation: those whose kClusterWarps-warp
+// CTAs fit two to an SM.
+__host__ __device__ constexpr bool tc_cluster_shape(int hd, int nt) { return hd <= 128 && nt == 1; }
 // Shared memory of the query fragments (the same for every warp of a CTA):
 // NT tiles x hd/16 k-steps x 2 words x 32 lanes.
 __host__ __device__ constexpr int tc_qfrag_bytes(int hd, int nt) { return nt * hd * 16; }
+// Shared memory after the page rings: the query fragments, the RoPE row of
+// the query's position (hd / 2 cos/sin pairs), the affine-K per-group q sums
+// ([nt][ng][4 heads]) and, for a fused append, the new K and V rows (up to
+// fp32) with the RoPE row of their position.
+__host__ __device__ constexpr int tc_pre_bytes(int hd, int nt, int ng) {
+  return tc_qfrag_bytes(hd, nt) + 4 * hd + 16 * nt * ng + 12 * hd;
+}
+
+// Fused append: quantizes the staged row (K rotated at its position) exactly
+// as the append kernel does.
+template <int HD>
+__device__ __forceinline__ RowCodes tc_append_row(const uint8_t* row, int act, const float2* cs, int rope,
+                                                  const PoolLayout& L, int lane) {
+  constexpr int DPL = HD / 32;
+  float x[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) x[j] = load_act(row, act, lane * DPL + j);
+  if (cs) rope_rotate_row<DPL>(x, cs, rope, lane);
+  return quantize_row<DPL>(x, L, lane);
+}
 
 // Shared-memory offset of 16-byte chunk `c` of row `r` in a block of rows of
 // ROWB bytes (32..256), with the chunk index XORed by a function of the row:
@@ -173,11 +201,13 @@ __device__ __forceinline__ float hilo_part(float x, int part) {
 // G <= 4, 2 for G = 8).  NG: scale groups per head (the same for K and V),
 // so every group index below is a compile-time constant.
 // PT: stored type of the scales (and biases) of K and V.
-template <int KK, int VK, int HD, int NT, int NG, int PT>
-__global__ void __launch_bounds__(kTcThreads, tc_min_blocks(HD, NT))
+// CL: the cluster mode (kClusterWarps warps per CTA, the chunks of a
+// (sequence, kv head) one cluster of A.cluster CTAs); else kWarps warps.
+template <int KK, int VK, int HD, int NT, int NG, int PT, bool CL>
+__global__ void __launch_bounds__(32 * (CL ? kClusterWarps : kWarps), CL ? 2 : tc_min_blocks(HD, NT))
 decode_tc_kernel(const __grid_constant__ TcArgs A) {
   constexpr int P = 16;
-  constexpr int NW = kWarps;
+  constexpr int NW = CL ? kClusterWarps : kWarps;
   constexpr int D = tc_depth(HD, NT);           // pages in flight per warp
   constexpr bool K8 = KK == KVQ_SYM_INT8, V8 = VK == KVQ_SYM_INT8;
   constexpr bool KAFF = KK == KVQ_AFFINE_INT4, VAFF = VK == KVQ_AFFINE_INT4;
@@ -216,17 +246,21 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   // for this grid to finish before it reads anything it writes.
   tc::grid_dependents_launch();
 
-  // One round of independent loads: the length, this lane's raw q elements
-  // (see the fragments below) and, for a whole-context decode, the block-table
-  // entries of the warp's pages, which do not depend on the length.
+  // One round of independent loads: the length, (warp 0) this lane's raw q
+  // elements (see the fragments below) and, for a whole-context decode, the
+  // block-table entries of the warp's pages, which do not depend on the length.
   const int64_t obase = ((int64_t)b * a.n_heads + (int64_t)kvh * G) * HD;
   const int L = a.seq_lens[b];
+  const int apos = a.app_pos ? a.app_pos[b] : -1;   // fused append: position of the new row
   float qv[NT][KCH][RUN];
+  if (warp == 0) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int hq = NT == 1 ? (gid >> 1) % G : 4 * nt + (gid >> 1);
+    for (int nt = 0; nt < NT; ++nt) {
+      const int hq = NT == 1 ? (gid >> 1) % G : 4 * nt + (gid >> 1);
 #pragma unroll
-    for (int c = 0; c < KCH; ++c) load_run<RUN>(a.q, a.act, obase + (int64_t)hq * HD + KDC * c + RUN * tig, qv[nt][c]);
+      for (int c = 0; c < KCH; ++c)
+        load_run<RUN>(a.q, a.act, obase + (int64_t)hq * HD + KDC * c + RUN * tig, qv[nt][c]);
+    }
   }
   const int CB = A.blocks_per_chunk;
   const int w = warp;
@@ -240,18 +274,21 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 
   int lo = 0, bad = 0;
   const int n_att = attended(a, L, &lo, &bad);
-  if (n_att <= 0) {
+  if (n_att <= 0) {   // the same for every CTA of a (sequence, kv head), so of a cluster
     if (chunk == 0) {
       if (bad && tid == 0 && kvh == 0) report(a.status, bad);
-      for (int i = tid; i < G * HD; i += kTcThreads) store_act(A.out, a.act, obase + i, 0.f);
+      for (int i = tid; i < G * HD; i += NW * 32) store_act(A.out, a.act, obase + i, 0.f);
     }
     return;
   }
   const int blk_lo = lo / P, blk_hi = (L + P - 1) / P;
   const int nch = (blk_hi - blk_lo + CB - 1) / CB;
-  if (chunk >= nch) return;
+  // In the cluster mode every CTA of the cluster reaches both cluster barriers
+  // below: a CTA past the sequence's last chunk reads no page and contributes
+  // an empty partial.
+  if (chunk >= nch && !CL) return;
   const int cb0 = blk_lo + chunk * CB;
-  const int ncb = min(CB, blk_hi - cb0);
+  const int ncb = chunk < nch ? min(CB, blk_hi - cb0) : 0;
   const int n_local = w < ncb ? (ncb - w + NW - 1) / NW : 0;   // pages w, w + NW, ... of the chunk
 
   // ---- page ring of this warp: D slots of SLOT bytes.  Lane (hl = lane % 16)
@@ -287,6 +324,96 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   const int64_t page_lane = vlane ? a.vl.page_bytes : a.kl.page_bytes;
   if (!whole && lane < n_local) ids = page_of(lane);
   ids = checked(ids, lane);
+  // Warp 0 copies the RoPE row of position L - 1 into shared memory ahead of
+  // every page copy (as its own, oldest commit group), so the row does not
+  // queue behind the pages and the query fragments are ready before they are.
+  const uint32_t qfs = tc::smem_u32(smem) + (uint32_t)(NW * D * SLOT);   // fragments
+  const uint32_t rope_s = qfs + tc_qfrag_bytes(HD, NT);                  // RoPE row
+  const uint32_t qsum_s = rope_s + 4 * HD;                                // affine-K q sums
+  if (warp == 0 && a.rope != KVQ_ROPE_NONE) {
+    const uint8_t* row = reinterpret_cast<const uint8_t*>(a.rope_tab) + (int64_t)(L - 1) * (4 * HD);
+    for (int j = lane; j < HD / 4; j += 32)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(rope_s + 16 * j), "l"(row + 16 * j) : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+
+  // ---- fused append.  The warp that reads the page of block apos / P (in
+  // the chunk that holds it) stages the new K and V rows and the RoPE row of
+  // their position in shared memory now, as its own commit group ahead of
+  // its pages.  When it reaches that page it quantizes the rows (tc_append_row,
+  // the append kernel's arithmetic) and writes them into the pool and over
+  // the row's stale copy in the page's slot, so no read of the pool has to
+  // wait for the write.  A position outside the attended blocks is written by
+  // warp 0 of chunk 0 in the prologue.
+  const int app_off = NW * D * SLOT + tc_qfrag_bytes(HD, NT) + 4 * HD + 16 * NT * NG;   // [K][V][RoPE]
+  int k_app = -1;    // this warp's page index of the new row; -2: write it in the prologue
+  int app_pg = -1;   // page id of the new row's block
+  if (a.app_pos) {
+    const bool pos_ok =
+        apos >= 0 && apos / P < a.max_pages && (a.rope == KVQ_ROPE_NONE || apos < a.rope_max_pos);
+    const int bp = apos / P;
+    if (!pos_ok) {
+      if (chunk == 0 && tid == 0) report(a.status, KVQ_DEV_BAD_POS);
+    } else if (bp >= blk_lo && bp < blk_hi) {
+      if (chunk == (bp - blk_lo) / CB && w == (bp - cb0) % NW) k_app = (bp - cb0) / NW;
+    } else if (chunk == 0 && w == 0) {
+      k_app = -2;
+    }
+    if (k_app != -1) {
+      app_pg = bt[bp];
+      if (app_pg < 0 || app_pg >= npp) {
+        report(a.status, KVQ_DEV_BAD_PAGE);
+        k_app = -1;
+      }
+    }
+    if (k_app != -1) {
+      const int actb = a.act == KVQ_F32 ? 4 : 2;
+      const int64_t row = ((int64_t)b * a.n_kv_heads + kvh) * HD * actb;
+      const uint8_t* ks = static_cast<const uint8_t*>(a.app_k) + row;
+      const uint8_t* vs = static_cast<const uint8_t*>(a.app_v) + row;
+      const uint8_t* cs = reinterpret_cast<const uint8_t*>(a.rope_tab) + (int64_t)apos * (4 * HD);
+      const uint32_t dst = tc::smem_u32(smem) + app_off;
+      for (int j = lane; j < HD * actb / 16; j += 32) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * j), "l"(ks + 16 * j) : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 4 * HD + 16 * j), "l"(vs + 16 * j)
+                     : "memory");
+      }
+      if (a.rope != KVQ_ROPE_NONE)
+        for (int j = lane; j < HD / 4; j += 32)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 8 * HD + 16 * j), "l"(cs + 16 * j)
+                       : "memory");
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+  }
+  // Quantizes the staged rows into the pool and, for s >= 0, into slot s.
+  auto write_app = [&](int s) {
+    const uint8_t* st = smem + app_off;
+    const float2* cs = a.rope != KVQ_ROPE_NONE ? reinterpret_cast<const float2*>(st + 8 * HD) : nullptr;
+    const int r = apos % P;
+    const RowCodes kq = tc_append_row<HD>(st, a.act, cs, a.rope, a.kl, lane);
+    const RowCodes vq = tc_append_row<HD>(st + 4 * HD, a.act, nullptr, a.rope, a.vl, lane);
+    store_row(kq, a.kl, const_cast<uint8_t*>(a.k_pool) + (int64_t)app_pg * a.kl.page_bytes + (int64_t)kvh * a.kl.sub_bytes,
+              r, lane);
+    store_row(vq, a.vl, const_cast<uint8_t*>(a.v_pool) + (int64_t)app_pg * a.vl.page_bytes + (int64_t)kvh * a.vl.sub_bytes,
+              r, lane);
+    if (s >= 0) {
+      uint8_t* slot = smem + (w * D + s) * SLOT;
+      const int jk = lane * kq.nbytes, jv = lane * vq.nbytes;
+      store_code_bytes(slot + swz<KRB>(r, jk / 16) + jk % 16, kq.w, kq.nbytes);
+      store_code_bytes(slot + KC + swz<VRB>(r, jv / 16) + jv % 16, vq.w, vq.nbytes);
+      uint8_t* kpr = slot + KC + VC + r * a.kl.param_row_bytes;
+      uint8_t* vpr = slot + KC + VC + KPMAX + r * a.vl.param_row_bytes;
+      if (kq.leader) {
+        store_param(kpr + param_scale_offset(a.kl, kq.group), a.kl.param, kq.scale);
+        if (KAFF) store_param(kpr + param_bias_offset(a.kl, kq.group), a.kl.param, kq.bias);
+      }
+      if (vq.leader) {
+        store_param(vpr + param_scale_offset(a.vl, vq.group), a.vl.param, vq.scale);
+        if (VAFF) store_param(vpr + param_bias_offset(a.vl, vq.group), a.vl.param, vq.bias);
+      }
+    }
+  };
+
   uint32_t valid = 0;   // bit s: slot s holds a page
   auto issue = [&](int k, int s) {   // all lanes: copies of page k into slot s
     if ((k & 31) == 0 && k > 0) ids = checked(k + lane < n_local ? page_of(k + lane) : -1, k + lane);
@@ -306,14 +433,17 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
 
-  // ---- query fragments.  Lane (gid, tig) holds, for column gid (head
-  // hq = gid / 2, part gid % 2), the q elements its K k-steps meet: the runs
-  // of RUN dims starting at KDC*c + RUN*tig of every K chunk c.
-  uint32_t qb[NT][KSTEPS][2];
-  float qsum[NT][KNG];   // affine K: sum of q over each group for the score head
-  {
+  // ---- query fragments (warp 0).  Lane (gid, tig) holds, for column gid
+  // (head hq = gid / 2, part gid % 2), the q elements its K k-steps meet: the
+  // runs of RUN dims starting at KDC*c + RUN*tig of every K chunk c.  They are
+  // the same for every warp of the CTA, so warp 0 keeps them in shared memory,
+  // [uint4 i][lane] with uint4 i = words of k-steps 2i, 2i+1, and every warp
+  // reloads the ones it needs per page (fewer live registers).
+  if (warp == 0) {
+    // the RoPE row: the oldest of this lane's D + 1 commit groups
+    asm volatile("cp.async.wait_group %0;" ::"n"(D) : "memory");
+    __syncwarp();
     const int part = gid & 1;
-    const float2* cs = reinterpret_cast<const float2*>(a.rope_tab) + (int64_t)(L - 1) * (HD / 2);
     const float sc = a.score_scale * kQScale;
     const int rope = a.rope;
 #pragma unroll
@@ -323,7 +453,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         for (int c = 0; c < KCH; ++c)
 #pragma unroll
           for (int k = 0; k < RUN; k += 2) {
-            const float2 t = cs[(KDC * c + RUN * tig + k) >> 1];
+            float2 t;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                         : "=f"(t.x), "=f"(t.y) : "r"(rope_s + 4 * (KDC * c + RUN * tig + k)) : "memory");
             const float x0 = qv[nt][c][k], x1 = qv[nt][c][k + 1];
             qv[nt][c][k] = x0 * t.x - x1 * t.y;
             qv[nt][c][k + 1] = x0 * t.y + x1 * t.x;
@@ -333,7 +465,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         for (int c = 0; c < KCH / 2; ++c)
 #pragma unroll
           for (int k = 0; k < RUN; ++k) {
-            const float2 t = cs[KDC * c + RUN * tig + k];
+            float2 t;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                         : "=f"(t.x), "=f"(t.y) : "r"(rope_s + 8 * (KDC * c + RUN * tig + k)) : "memory");
             const float x0 = qv[nt][c][k], x1 = qv[nt][c + KCH / 2][k];
             qv[nt][c][k] = x0 * t.x - x1 * t.y;
             qv[nt][c + KCH / 2][k] = x0 * t.y + x1 * t.x;
@@ -346,25 +480,30 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       // B fragments: 4-bit K chunk c, parity p (p = 1 meets 16 * code, so q / 16):
       //   b0 = q at dims KDC*c + 8tig + p + {0, 4},  b1 = dims + {2, 6}
       // 8-bit K chunk c:  b0 = dims 16c + 4tig + {0, 2},  b1 = dims + {1, 3}
+      uint32_t qb[KSTEPS][2];
 #pragma unroll
       for (int c = 0; c < KCH; ++c) {
         if constexpr (K8) {
-          qb[nt][c][0] = tc::pack_half2(hilo_part(qv[nt][c][0], part), hilo_part(qv[nt][c][2], part));
-          qb[nt][c][1] = tc::pack_half2(hilo_part(qv[nt][c][1], part), hilo_part(qv[nt][c][3], part));
+          qb[c][0] = tc::pack_half2(hilo_part(qv[nt][c][0], part), hilo_part(qv[nt][c][2], part));
+          qb[c][1] = tc::pack_half2(hilo_part(qv[nt][c][1], part), hilo_part(qv[nt][c][3], part));
         } else {
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             const float f = p ? 1.0f / 16.0f : 1.0f;
-            qb[nt][2 * c + p][0] =
+            qb[2 * c + p][0] =
                 tc::pack_half2(hilo_part(qv[nt][c][p] * f, part), hilo_part(qv[nt][c][p + 4] * f, part));
-            qb[nt][2 * c + p][1] =
+            qb[2 * c + p][1] =
                 tc::pack_half2(hilo_part(qv[nt][c][p + 2] * f, part), hilo_part(qv[nt][c][p + 6] * f, part));
           }
         }
       }
-      // affine K: per-group q sums, gathered for the lane's score head 4nt + tig
 #pragma unroll
-      for (int g = 0; g < KNG; ++g) qsum[nt][g] = 0.f;
+      for (int i = 0; i < KSTEPS / 2; ++i)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qfs + ((nt * (KSTEPS / 2) + i) * 32 + lane) * 16),
+                     "r"(qb[2 * i][0]), "r"(qb[2 * i][1]), "r"(qb[2 * i + 1][0]), "r"(qb[2 * i + 1][1])
+                     : "memory");
+      // affine K: per-group q sums of the tile's heads, [nt][g][4] (lane 8h holds
+      // head h of the tile: gid = 2h, part hi)
       if constexpr (KAFF) {
         float part_sum[KNG];
 #pragma unroll
@@ -383,29 +522,29 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
           float v = part_sum[g];
           v += __shfl_xor_sync(0xffffffffu, v, 1);
           v += __shfl_xor_sync(0xffffffffu, v, 2);
-          // lane 8h holds head h (gid = 2h, part hi) of this tile
-          const int hs = NT == 1 ? tig % G : tig;
-          qsum[nt][g] = __shfl_sync(0xffffffffu, v, 8 * hs) * (1.0f / kQScale);
+          if (tig == 0 && (gid & 1) == 0)
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(qsum_s + 4 * ((nt * KNG + g) * 4 + (gid >> 1))),
+                         "f"(v * (1.0f / kQScale))
+                         : "memory");
         }
       }
     }
   }
-
-  // The fragments are the same for every warp of the CTA: warp 0 keeps them in
-  // shared memory, [uint4 i][lane] with uint4 i = words of k-steps 2i, 2i+1,
-  // and every warp reloads the ones it needs per page (fewer live registers).
-  const uint32_t qfs = tc::smem_u32(smem) + (uint32_t)(NW * D * SLOT);
-  if (warp == 0) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < KSTEPS / 2; ++i)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qfs + ((nt * (KSTEPS / 2) + i) * 32 + lane) * 16),
-                     "r"(qb[nt][2 * i][0]), "r"(qb[nt][2 * i][1]), "r"(qb[nt][2 * i + 1][0]),
-                     "r"(qb[nt][2 * i + 1][1])
-                     : "memory");
-  }
+  if (k_app == -2) write_app(-1);   // warp 0, past its wait for the staged rows above
   __syncthreads();
+  // affine K: the q sums of this lane's score head 4nt + tig (mod G)
+  float qsum[NT][KNG];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int g = 0; g < KNG; ++g) {
+      qsum[nt][g] = 0.f;
+      if constexpr (KAFF) {
+        const int hs = NT == 1 ? tig % G : tig;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qsum[nt][g]) : "r"(qsum_s + 4 * ((nt * KNG + g) * 4 + hs))
+                     : "memory");
+      }
+    }
 
   // ---- per-lane constants of the main loop
   const int kprb = a.kl.param_row_bytes, vprb = a.vl.param_row_bytes;
@@ -450,6 +589,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     // and the warp's lanes see each other's copies after the sync
     asm volatile("cp.async.wait_group %0;" ::"n"(D - 1) : "memory");
     __syncwarp();
+    if (k == k_app) {   // the new row's page (its staged rows landed before it)
+      write_app(s);
+      __syncwarp();
+    }
     if ((valid >> s) & 1u) {
       const uint32_t kc = wring + s * SLOT;
       const uint32_t vc = kc + KC;
@@ -736,6 +879,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   __syncthreads();
 
   const int64_t cidx = ((int64_t)b * a.n_kv_heads + kvh) * a.n_chunks + chunk;
+  // cluster mode: the CTA's merged partial stays in its own shared memory,
+  // o [G][HD] then (M, l) [G], after the warps' states
+  const uint32_t cpart = tc::smem_u32(smem) + (((uint32_t)(NW * G * HD + 2 * NW * G) * 4 + 15) & ~15u);
+  const uint32_t cml = cpart + 4 * G * HD;
   for (int i = tid; i < G * HD; i += NW * 32) {
     const int h = i / HD, d = i - h * HD;
     float M = mws[h];
@@ -750,7 +897,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         ls = fmaf(f, lws[w2 * G + h], ls);
       }
     }
-    if (nch == 1) {
+    if constexpr (CL) {
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(cpart + 4 * i), "f"(o) : "memory");
+      if (d == 0) asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(cml + 8 * h), "f"(M), "f"(ls) : "memory");
+    } else if (nch == 1) {
       store_act(A.out, a.act, obase + i, ls > 0.f ? o / ls : 0.f);
     } else {
       a.ws_acc[(cidx * G + h) * HD + d] = o;
@@ -759,6 +909,49 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         a.ws_ml[(cidx * G + h) * 2 + 1] = ls;
       }
     }
+  }
+
+  // ---- cluster mode: log-sum-exp combine over distributed shared memory.
+  // After the first cluster barrier every CTA's partial is visible to the
+  // cluster; CTA r then combines its slice of the G * HD outputs from the
+  // partials of all A.cluster CTAs, and the second barrier keeps every CTA's
+  // shared memory alive until the whole cluster is done reading it.
+  if constexpr (CL) {
+    tc::cluster_barrier();
+    const int nc = A.cluster;
+    const int E = G * HD;
+    const int per = (E + nc - 1) / nc;
+    const int e0 = (int)tc::cluster_rank() * per;
+    const int e1 = min(E, e0 + per);
+    for (int e = e0 + tid; e < e1; e += NW * 32) {
+      const int h = e / HD;
+      float2 ml[kMaxCluster];
+      float v[kMaxCluster];
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) {
+        ml[c] = make_float2(-INFINITY, 0.f);
+        v[c] = 0.f;
+        if (c < nc) {
+          ml[c] = tc::ld_cluster_f2(tc::cluster_addr(cml + 8 * h, c));
+          v[c] = tc::ld_cluster_f(tc::cluster_addr(cpart + 4 * e, c));
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMaxCluster; ++c) mx = fmaxf(mx, ml[c].x);
+      float num = 0.f, den = 0.f;
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) {
+          const float wt = exp2f(ml[c].x - mx);   // 0 for an empty partial (-inf)
+          num = fmaf(wt, v[c], num);
+          den = fmaf(wt, ml[c].y, den);
+        }
+      }
+      store_act(A.out, a.act, obase + e, den > 0.f ? num / den : 0.f);
+    }
+    tc::cluster_barrier();
+    return;
   }
   if (nch == 1) return;
 
@@ -874,28 +1067,63 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   if (tid == 0) *counter = 0;   // ready for the next call
 }
 
-// Host launcher of one instantiation (dynamic shared memory, optional PDL).
-template <int KK, int VK, int HD, int NT, int NG, int PT>
-kvq_status launch_tc_one(const TcArgs& t, dim3 grid, size_t smem, cudaStream_t stream, bool pdl) {
-  auto kern = decode_tc_kernel<KK, VK, HD, NT, NG, PT>;
+// How to launch the kernel: grid and dynamic shared memory, warps per CTA,
+// CTAs per cluster (0: no cluster), PDL.  With max_active set, nothing is
+// launched: it receives how many such clusters can be resident at once.
+struct TcLaunchCfg {
+  dim3 grid;
+  size_t smem;
+  cudaStream_t stream;
+  bool pdl;
+  int warps;
+  int cluster;
+  int* max_active;
+};
+
+// Host launcher of one instantiation.
+template <int KK, int VK, int HD, int NT, int NG, int PT, bool CL>
+kvq_status launch_tc_one(const TcArgs& t, const TcLaunchCfg& lc) {
+  auto kern = decode_tc_kernel<KK, VK, HD, NT, NG, PT, CL>;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     attr_done[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = lc.grid;
+  cfg.blockDim = dim3(32 * lc.warps);
+  cfg.dynamicSmemBytes = lc.smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (lc.cluster > 0) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = (unsigned)lc.cluster;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (lc.pdl) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = at;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
+  if (lc.max_active) {
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) {
+      cudaGetLastError();   // a refused configuration is an answer, not a sticky error
+      n = 0;
+    }
+    *lc.max_active = n;
+    return KVQ_OK;
+  }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, t);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
@@ -910,11 +1138,14 @@ inline bool tc_has_shape(int head_dim, int nt, int ng) {
 }
 
 template <int KK, int VK, int PT>
-kvq_status launch_tc_pt(const TcArgs& t, int head_dim, int nt, int ng, dim3 grid, size_t smem,
-                        cudaStream_t stream, bool pdl) {
-#define KVQ_TC(HD_, NT_, NG_)                                          \
-  if (head_dim == HD_ && nt == NT_ && ng == NG_)                       \
-    return launch_tc_one<KK, VK, HD_, NT_, NG_, PT>(t, grid, smem, stream, pdl);
+kvq_status launch_tc_pt(const TcArgs& t, int head_dim, int nt, int ng, const TcLaunchCfg& lc) {
+#define KVQ_TC(HD_, NT_, NG_)                                                                      \
+  if (head_dim == HD_ && nt == NT_ && ng == NG_) {                                                 \
+    if constexpr (tc_cluster_shape(HD_, NT_))                                                       \
+      if (lc.cluster > 0) return launch_tc_one<KK, VK, HD_, NT_, NG_, PT, true>(t, lc);            \
+    if (lc.cluster > 0) return fail(KVQ_ERR_UNSUPPORTED, "no cluster-mode kernel for this shape");  \
+    return launch_tc_one<KK, VK, HD_, NT_, NG_, PT, false>(t, lc);                                 \
+  }
   KVQ_TC(64, 1, 1)
   KVQ_TC(64, 1, 2)
   KVQ_TC(128, 1, 1)
@@ -932,8 +1163,8 @@ kvq_status launch_tc_pt(const TcArgs& t, int head_dim, int nt, int ng, dim3 grid
 }
 
 // One launcher per (K/V kind pair, scale type), each its own translation unit.
-typedef kvq_status (*TcLaunch)(const TcArgs&, int, int, int, dim3, size_t, cudaStream_t, bool);
-#define KVQ_TC_DECLARE(NAME) kvq_status NAME(const TcArgs&, int, int, int, dim3, size_t, cudaStream_t, bool);
+typedef kvq_status (*TcLaunch)(const TcArgs&, int, int, int, const TcLaunchCfg&);
+#define KVQ_TC_DECLARE(NAME) kvq_status NAME(const TcArgs&, int, int, int, const TcLaunchCfg&);
 KVQ_TC_DECLARE(launch_tc_s4s4_f32)
 KVQ_TC_DECLARE(launch_tc_s4s4_f16)
 KVQ_TC_DECLARE(launch_tc_s4s4_bf16)

@@ -3,8 +3,7 @@
 #include "kvq_decode_tc.cuh"
 
 namespace kvq {
-kvq_status launch_tc_s8s8_bf16(const TcArgs& t, int hd, int nt, int ng, dim3 grid, size_t smem,
-                           cudaStream_t s, bool pdl) {
-  return launch_tc_pt<KVQ_SYM_INT8, KVQ_SYM_INT8, KVQ_BF16>(t, hd, nt, ng, grid, smem, s, pdl);
+kvq_status launch_tc_s8s8_bf16(const TcArgs& t, int hd, int nt, int ng, const TcLaunchCfg& lc) {
+  return launch_tc_pt<KVQ_SYM_INT8, KVQ_SYM_INT8, KVQ_BF16>(t, hd, nt, ng, lc);
 }
 }  // namespace kvq

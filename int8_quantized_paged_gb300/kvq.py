@@ -62,6 +62,7 @@ _SIGS = {
     "kvq_last_error": (C.c_char_p, []),
     "kvq_validate_config": (C.c_int, [_cfgp]),
     "kvq_decode_launches": (_i32, [_cfgp]),
+    "kvq_decode_cluster_ctas": (_i32, [_cfgp, _i32, _i32, _i32, _i32]),
     "kvq_cache_bytes": (_sz, [_cfgp, _i32, _i64]),
     "kvq_page_bytes": (_sz, [_cfgp, _i32]),
     "kvq_pool_create": (C.c_int, [_i32, C.POINTER(_vp)]),
@@ -82,6 +83,9 @@ _SIGS = {
     "kvq_decode_workspace_bytes": (_sz, [_cfgp, _i32, _i32, _i32]),
     "kvq_decode_attention": (C.c_int, [_cfgp, _i32, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp,
                                        _i32, _vp, _vp, _sz, _i32, _vp, _vp]),
+    "kvq_append_decode_attention": (C.c_int, [_cfgp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
+                                              _vp, _vp, _i32, _vp, _vp, _sz, _i32, _vp, _vp]),
+    "kvq_append_decode_launches": (_i32, [_cfgp]),
     "kvq_window_workspace_bytes": (_sz, [_cfgp, _i32, _i32, _i32]),
     "kvq_window_decode": (C.c_int, [_cfgp, _i32, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp, _vp,
                                     _i32, _vp, _vp, _sz, _i32, _vp, _vp]),
@@ -151,6 +155,15 @@ def decode_launches(cfg: Config) -> int:
     """Kernel launches per decode call (1: tensor-core path, 2: CUDA-core path)."""
     n = lib().kvq_decode_launches(C.byref(cfg))
     if n == 0:
+        raise KvqError(ERR_INVALID_ARG, last_error())
+    return n
+
+
+def decode_cluster_ctas(cfg: Config, batch: int, max_pages_per_seq: int, window: int = 0,
+                        chunk_tokens: int = 0) -> int:
+    """CTAs per cluster of a decode call (0: the partials go through the workspace)."""
+    n = lib().kvq_decode_cluster_ctas(C.byref(cfg), batch, max_pages_per_seq, window, chunk_tokens)
+    if n < 0:
         raise KvqError(ERR_INVALID_ARG, last_error())
     return n
 
@@ -276,6 +289,25 @@ def decode_attention(cfg: Config, q, k_pool, v_pool, n_pool_pages: int, block_ta
         C.byref(cfg), q.shape[0], _ptr(q), _ptr(k_pool), _ptr(v_pool), n_pool_pages, _ptr(block_table),
         max_pages_per_seq, _ptr(seq_lens), _ptr(rope_tab), rope_max_pos, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), chunk_tokens, _ptr(dev_status), _stream(stream)))
+
+
+def append_decode_attention(cfg: Config, q, k_new, v_new, pos, k_pool, v_pool, n_pool_pages: int,
+                            block_table, max_pages_per_seq: int, seq_lens, rope_tab, rope_max_pos: int,
+                            out, workspace, dev_status, chunk_tokens: int = 0, stream=None) -> None:
+    """kvq_append of row b at pos[b] for every sequence b, then kvq_decode_attention, in one call."""
+    _check(lib().kvq_append_decode_attention(
+        C.byref(cfg), q.shape[0], _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(k_pool), _ptr(v_pool),
+        n_pool_pages, _ptr(block_table), max_pages_per_seq, _ptr(seq_lens), _ptr(rope_tab), rope_max_pos,
+        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), chunk_tokens,
+        _ptr(dev_status), _stream(stream)))
+
+
+def append_decode_launches(cfg: Config) -> int:
+    """Kernel launches per append_decode_attention call (1: tensor-core path)."""
+    n = lib().kvq_append_decode_launches(C.byref(cfg))
+    if n == 0:
+        raise KvqError(ERR_INVALID_ARG, last_error())
+    return n
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
