@@ -299,12 +299,16 @@ class BenchLayer:
             self.cache.decode(self.q, self.seq_lens, self.out, self.ws, self.chunk)
 
     def fused(self) -> bool:
-        """Whether step() makes one kvq_append_decode_attention call (whole-context layers)."""
-        return self.use_fused and not self.window
+        """Whether step() makes one fused call (kvq_append_decode_attention or
+        kvq_append_window_decode)."""
+        return self.use_fused
 
     def step(self):
         """This layer's share of a decode step: append the new row, then decode."""
-        if self.fused():
+        if self.fused() and self.window:
+            self.cache.append_window_decode(self.q, self.k_new, self.v_new, self.pos, self.seq_lens, self.out,
+                                            self.ws, self.window, self.chunk)
+        elif self.fused():
             self.cache.append_decode(self.q, self.k_new, self.v_new, self.pos, self.seq_lens, self.out, self.ws,
                                      self.chunk)
         else:
@@ -504,8 +508,8 @@ def run_gpu(args) -> dict | None:
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "graph": "CUDA graph of one step",
             "chunk_tokens": args.chunk_tokens or "library default",
-            "step_call": ("kvq_append_decode_attention (window layers: kvq_append + kvq_window_decode)"
-                          if fused else "kvq_append + kvq_decode_attention"),
+            "step_call": ("kvq_append_decode_attention (window layers: kvq_append_window_decode)"
+                          if fused else "kvq_append + kvq_decode_attention (window layers: kvq_window_decode)"),
         },
         "tokens_per_s": round(whole_job(query_tokens, world, ms_max), 1),
         "context_tokens_per_s": round(whole_job(ctx_tokens, world, ms_max), 1),

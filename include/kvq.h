@@ -324,9 +324,24 @@ kvq_status kvq_append_decode_attention(const kvq_config* cfg, int32_t batch, con
                                        const float* rope_tab, int32_t rope_max_pos,
                                        void* out, void* workspace, size_t workspace_bytes,
                                        int32_t chunk_tokens, int32_t* dev_status, kvq_stream_t stream);
-/* Kernel launches of one kvq_append_decode_attention call for cfg: 1 on the
- * tensor-core path, 3 on the CUDA-core path; 0 for an invalid config. */
+/* Kernel launches of one kvq_append_decode_attention (or
+ * kvq_append_window_decode) call for cfg: 1 on the tensor-core path, 3 on the
+ * CUDA-core path; 0 for an invalid config. */
 int32_t kvq_append_decode_launches(const kvq_config* cfg);
+
+/* The same fused step for a sliding-window layer: kvq_append of row b at
+ * pos[b] into ring row pos[b] mod ring_rows, then kvq_window_decode.  With
+ * window <= ring_rows no attended key shares the new row's ring row.
+ * Arguments as in kvq_window_decode plus k_new, v_new and pos as in
+ * kvq_append_decode_attention. */
+kvq_status kvq_append_window_decode(const kvq_config* cfg, int32_t batch, const void* q,
+                                    const void* k_new, const void* v_new, const int32_t* pos,
+                                    void* k_pool, void* v_pool, int32_t n_pool_pages,
+                                    const int32_t* ring_table, int32_t ring_rows, int32_t window,
+                                    const int32_t* seq_lens,
+                                    const float* rope_tab, int32_t rope_max_pos,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    int32_t chunk_tokens, int32_t* dev_status, kvq_stream_t stream);
 
 /* ------------------------------------------- decode without allocation --
  * The pages have no counterpart to this entry point.  It exists for callers

@@ -77,6 +77,13 @@ class LayerCache:
                                     self.block_table, self.max_pages, seq_lens, self.rope_tab, self.rope_max_pos,
                                     out, workspace, self.status, chunk_tokens, stream)
 
+    def append_window_decode(self, q, k_new, v_new, pos, seq_lens, out, workspace, window: int,
+                             chunk_tokens: int = 0, stream=None) -> None:
+        """Append row b at pos[b] into the ring of every sequence b, then window-decode (one call)."""
+        kvq.append_window_decode(self.cfg, q, k_new, v_new, pos, self.k_pool, self.v_pool, self.n_pool_pages,
+                                 self.block_table, self.ring_rows, window, seq_lens, self.rope_tab,
+                                 self.rope_max_pos, out, workspace, self.status, chunk_tokens, stream)
+
     def window_decode(self, q, seq_lens, out, workspace, window: int, chunk_tokens: int = 0,
                       stream=None) -> None:
         kvq.window_decode(self.cfg, q, self.k_pool, self.v_pool, self.n_pool_pages, self.block_table,

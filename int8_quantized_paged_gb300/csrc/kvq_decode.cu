@@ -478,6 +478,40 @@ extern "C" kvq_status kvq_append_decode_attention(const kvq_config* cfg, int32_t
                     (cudaStream_t)stream, 0, 0, (int64_t)max_pages_per_seq * cfg->page_size, k_new, v_new, pos);
 }
 
+extern "C" kvq_status kvq_append_window_decode(const kvq_config* cfg, int32_t batch, const void* q,
+                                               const void* k_new, const void* v_new, const int32_t* pos,
+                                               void* k_pool, void* v_pool, int32_t n_pool_pages,
+                                               const int32_t* ring_table, int32_t ring_rows, int32_t window,
+                                               const int32_t* seq_lens, const float* rope_tab,
+                                               int32_t rope_max_pos, void* out, void* workspace,
+                                               size_t workspace_bytes, int32_t chunk_tokens,
+                                               int32_t* dev_status, kvq_stream_t stream) {
+  clear_error();
+  kvq_status st = check_decode_args(cfg, batch, q, k_pool, v_pool, n_pool_pages, ring_table, seq_lens,
+                                    rope_tab, rope_max_pos, out, workspace, chunk_tokens, dev_status);
+  if (st != KVQ_OK || batch == 0) return st;
+  if (ring_rows < cfg->page_size || ring_rows % cfg->page_size != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "ring_rows %d must be a positive multiple of page_size", ring_rows);
+  if (window < 1 || window > ring_rows)
+    return fail(KVQ_ERR_INVALID_ARG, "window %d must be in [1, ring_rows=%d]", window, ring_rows);
+  if (!k_new || !v_new || !pos) return fail(KVQ_ERR_INVALID_ARG, "k_new, v_new and pos must not be NULL");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+    return fail(KVQ_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  const int32_t max_pages = ring_rows / cfg->page_size;
+  if (!tc_enabled(*cfg)) {
+    // The CUDA-core decode has no fused append: the append kernel, then the decode.
+    st = kvq_append(cfg, batch, k_new, v_new, nullptr, pos, ring_table, batch, max_pages, ring_rows, rope_tab,
+                    rope_max_pos, k_pool, v_pool, n_pool_pages, dev_status, stream);
+    if (st != KVQ_OK) return st;
+    return run_decode(cfg, batch, q, k_pool, v_pool, n_pool_pages, ring_table, max_pages, seq_lens, rope_tab,
+                      rope_max_pos, out, workspace, workspace_bytes, chunk_tokens, dev_status, (cudaStream_t)stream,
+                      ring_rows, window, window);
+  }
+  return run_decode(cfg, batch, q, k_pool, v_pool, n_pool_pages, ring_table, max_pages, seq_lens, rope_tab,
+                    rope_max_pos, out, workspace, workspace_bytes, chunk_tokens, dev_status, (cudaStream_t)stream,
+                    ring_rows, window, window, k_new, v_new, pos);
+}
+
 extern "C" kvq_status kvq_decode_attention(const kvq_config* cfg, int32_t batch, const void* q,
                                            const void* k_pool, const void* v_pool, int32_t n_pool_pages,
                                            const int32_t* block_table, int32_t max_pages_per_seq,

@@ -39,9 +39,10 @@ struct DecodeArgs {
   const int32_t* block_table;
   const int32_t* seq_lens;
   const float* rope_tab;
-  // Fused append (tensor-core whole-context decode only; NULL otherwise): the
-  // new K/V rows [batch][n_kv_heads][HD] of act type and their positions,
-  // quantized into the pools before the decode reads them.
+  // Fused append (tensor-core decode only; NULL otherwise): the new K/V rows
+  // [batch][n_kv_heads][HD] of act type and their positions, quantized into
+  // the pools (for a ring, into row pos mod ring_rows) before the decode reads
+  // them.
   const void* app_k;
   const void* app_v;
   const int32_t* app_pos;

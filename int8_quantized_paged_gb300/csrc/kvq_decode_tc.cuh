@@ -79,11 +79,12 @@ constexpr float kWScale = 128.0f;   // w is held x 2^7 (w <= 2^8 * 2^7 < 65504)
 constexpr float kLazyMax = 8.0f;    // raise the running max only past +2^8
 
 // Pages in flight per warp, and CTAs per SM (the launch bounds), by shape.
-__host__ __device__ constexpr int tc_depth(int hd, int nt) { return hd == 256 ? 3 : 4; }
-__host__ __device__ constexpr int tc_min_blocks(int hd, int nt) { return (hd <= 128 && nt == 1) ? 5 : 3; }
-// Shapes with a cluster-mode instantiation: those whose kClusterWarps-warp
-// CTAs fit two to an SM.
-__host__ __device__ constexpr bool tc_cluster_shape(int hd, int nt) { return hd <= 128 && nt == 1; }
+__host__ __device__ constexpr int tc_depth(int hd, int nt) { return (hd == 256 || nt == 2) ? 3 : 4; }
+__host__ __device__ constexpr int tc_min_blocks(int hd, int nt) { return hd <= 128 ? (nt == 1 ? 5 : 4) : 3; }
+// Shapes with a cluster-mode instantiation (one 8-column tile: G <= 4), and
+// the cluster-mode CTAs resident per SM.
+__host__ __device__ constexpr bool tc_cluster_shape(int hd, int nt) { return nt == 1; }
+__host__ __device__ constexpr int tc_cluster_min_blocks(int hd) { return hd <= 128 ? 2 : 1; }
 // Shared memory of the query fragments (the same for every warp of a CTA):
 // NT tiles x hd/16 k-steps x 2 words x 32 lanes.
 __host__ __device__ constexpr int tc_qfrag_bytes(int hd, int nt) { return nt * hd * 16; }
@@ -204,7 +205,8 @@ __device__ __forceinline__ float hilo_part(float x, int part) {
 // CL: the cluster mode (kClusterWarps warps per CTA, the chunks of a
 // (sequence, kv head) one cluster of A.cluster CTAs); else kWarps warps.
 template <int KK, int VK, int HD, int NT, int NG, int PT, bool CL>
-__global__ void __launch_bounds__(32 * (CL ? kClusterWarps : kWarps), CL ? 2 : tc_min_blocks(HD, NT))
+__global__ void __launch_bounds__(32 * (CL ? kClusterWarps : kWarps),
+                                   CL ? tc_cluster_min_blocks(HD) : tc_min_blocks(HD, NT))
 decode_tc_kernel(const __grid_constant__ TcArgs A) {
   constexpr int P = 16;
   constexpr int NW = CL ? kClusterWarps : kWarps;
@@ -337,8 +339,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
 
-  // ---- fused append.  The warp that reads the page of block apos / P (in
-  // the chunk that holds it) stages the new K and V rows and the RoPE row of
+  // ---- fused append.  The warp that reads the page of absolute block
+  // apos / P (in the chunk that holds it; for a ring, the ring page that block
+  // lives in, whose other rows a window no longer than the ring reads only
+  // through the same block) stages the new K and V rows and the RoPE row of
   // their position in shared memory now, as its own commit group ahead of
   // its pages.  When it reaches that page it quantizes the rows (tc_append_row,
   // the append kernel's arithmetic) and writes them into the pool and over
@@ -349,8 +353,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   int k_app = -1;    // this warp's page index of the new row; -2: write it in the prologue
   int app_pg = -1;   // page id of the new row's block
   if (a.app_pos) {
-    const bool pos_ok =
-        apos >= 0 && apos / P < a.max_pages && (a.rope == KVQ_ROPE_NONE || apos < a.rope_max_pos);
+    const bool pos_ok = apos >= 0 && (ring > 0 || apos / P < a.max_pages) &&
+                        (a.rope == KVQ_ROPE_NONE || apos < a.rope_max_pos);
     const int bp = apos / P;
     if (!pos_ok) {
       if (chunk == 0 && tid == 0) report(a.status, KVQ_DEV_BAD_POS);
@@ -360,7 +364,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       k_app = -2;
     }
     if (k_app != -1) {
-      app_pg = bt[bp];
+      app_pg = bt[ring > 0 ? (int)(((int64_t)bp * P) % ring) / P : bp];   // a ring keeps the block in a ring page
       if (app_pg < 0 || app_pg >= npp) {
         report(a.status, KVQ_DEV_BAD_PAGE);
         k_app = -1;

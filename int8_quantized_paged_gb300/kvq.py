@@ -86,6 +86,8 @@ _SIGS = {
     "kvq_append_decode_attention": (C.c_int, [_cfgp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
                                               _vp, _vp, _i32, _vp, _vp, _sz, _i32, _vp, _vp]),
     "kvq_append_decode_launches": (_i32, [_cfgp]),
+    "kvq_append_window_decode": (C.c_int, [_cfgp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
+                                           _vp, _vp, _i32, _vp, _vp, _sz, _i32, _vp, _vp]),
     "kvq_window_workspace_bytes": (_sz, [_cfgp, _i32, _i32, _i32]),
     "kvq_window_decode": (C.c_int, [_cfgp, _i32, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp, _vp,
                                     _i32, _vp, _vp, _sz, _i32, _vp, _vp]),
@@ -298,6 +300,17 @@ def append_decode_attention(cfg: Config, q, k_new, v_new, pos, k_pool, v_pool, n
     _check(lib().kvq_append_decode_attention(
         C.byref(cfg), q.shape[0], _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(k_pool), _ptr(v_pool),
         n_pool_pages, _ptr(block_table), max_pages_per_seq, _ptr(seq_lens), _ptr(rope_tab), rope_max_pos,
+        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), chunk_tokens,
+        _ptr(dev_status), _stream(stream)))
+
+
+def append_window_decode(cfg: Config, q, k_new, v_new, pos, k_pool, v_pool, n_pool_pages: int, ring_table,
+                         ring_rows: int, window: int, seq_lens, rope_tab, rope_max_pos: int, out, workspace,
+                         dev_status, chunk_tokens: int = 0, stream=None) -> None:
+    """kvq_append into the ring of row b at pos[b] for every sequence b, then kvq_window_decode."""
+    _check(lib().kvq_append_window_decode(
+        C.byref(cfg), q.shape[0], _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(k_pool), _ptr(v_pool),
+        n_pool_pages, _ptr(ring_table), ring_rows, window, _ptr(seq_lens), _ptr(rope_tab), rope_max_pos,
         _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), chunk_tokens,
         _ptr(dev_status), _stream(stream)))
 

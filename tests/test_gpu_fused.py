@@ -141,3 +141,42 @@ def test_fused_argument_checks():
         kvq.append_decode_attention(c.cfg, q, k_bad, k_bad, None, c.cache.k_pool, c.cache.v_pool,
                                     c.n_pages, c.cache.block_table, c.max_pages, lens, c.cache.rope_tab,
                                     c.rope_max, out, ws, c.cache.status)
+
+
+def _window_step(c: Case, window: int, chunk: int, step: int = 1):
+    dev = c.cache.device
+    k_new = wl.new_rows(c.w, "k", c.B, step=step)
+    v_new = wl.new_rows(c.w, "v", c.B, step=step)
+    q = c.queries(step=step)
+    qt = torch.from_numpy(q).to(dev)
+    out = torch.full_like(qt, float("nan"))
+    ws = c.cache.workspace(c.B, chunk, window)
+    pos = (c.lens - 1).astype(np.int32)
+    c.cache.append_window_decode(qt, torch.from_numpy(k_new).to(dev), torch.from_numpy(v_new).to(dev),
+                                 torch.from_numpy(pos).to(dev), torch.from_numpy(c.lens).to(dev), out, ws,
+                                 window, chunk)
+    torch.cuda.synchronize()
+    return q, out.float().cpu().numpy().astype(np.float64), k_new, v_new, pos
+
+
+@pytest.mark.parametrize("chunk", [0, 64])
+@pytest.mark.parametrize("L", [5, 1024, 1153, 3000])
+def test_fused_window_step_matches_oracle(L, chunk):
+    """Ring of 1152 rows, window 1024: the new row overwrites ring row (L-1) mod 1152."""
+    w = wl.workload("gemma_mix", batch=1)
+    c = Case(w, [L], ring_rows=1152)
+    q, got, k_new, v_new, pos = _window_step(c, 1024, chunk)
+    assert c.cache.status_bits() == 0
+    s = c.spec
+    O.append(s, c.pools, k_new, v_new, np.array([0]), pos, c.bt, 1152, oracle_rope(s.head_dim, s.rope_base,
+                                                                                      c.rope_max))
+    k, v = c.gpu_pools()
+    assert np.array_equal(k, c.pools["k"]) and np.array_equal(v, c.pools["v"])
+    assert max_row_err(got, c.oracle_decode(q, window=1024)) <= TOL
+    assert np.array_equal(got, c.gpu_decode(q, chunk_tokens=chunk, window=1024))
+
+
+def test_window_uses_the_cluster_mode():
+    w = wl.workload("gemma_mix", batch=1)
+    cfg = kvq.config(**w)
+    assert kvq.decode_cluster_ctas(cfg, 1, 1152 // 16, window=1024) > 0
