@@ -109,10 +109,12 @@ static size_t tc_ring_bytes(const kvq_config& c) {
 }
 
 // The cluster mode: a few sequences, each short enough that one cluster of
-// up to kMaxCluster CTAs of kClusterWarps warps covers it with about four
-// pages per warp (at most eight), and all the clusters resident at once.  On
-// success fills the launch configuration (grid, shared memory, warps, cluster
-// size) and the 16-token blocks per CTA.
+// up to kMaxCluster CTAs of kClusterWarps warps covers it with at most eight
+// pages per warp, and all the clusters resident at once.  The cluster is as
+// large as that allows, down to one page per warp: the pages of a short
+// context spread over as many SMs as possible.  On success fills the launch
+// configuration (grid, shared memory, warps, cluster size) and the 16-token
+// blocks per CTA.
 static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens, int32_t window, TcLaunch fn,
                          size_t ring, size_t pre, TcLaunchCfg* lc, int* cb_out) {
   const int G = c.n_heads / c.n_kv_heads;
@@ -121,30 +123,35 @@ static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens,
   if (!cluster_enabled() || batch < 1 || !tc_cluster_shape(hd, nt)) return false;
   // blocks of the longest context (a window may start mid-page)
   const int64_t blocks = (max_tokens + c.page_size - 1) / c.page_size + (window > 0 ? 1 : 0);
-  if (blocks > (int64_t)kMaxCluster * kClusterWarps * 8 || (int64_t)batch * c.n_kv_heads > 4 * num_sms())
+  const int64_t max_ppw = 8;
+  if (blocks > (int64_t)kMaxCluster * kClusterWarps * max_ppw || (int64_t)batch * c.n_kv_heads > 4 * num_sms())
     return false;
-  const int64_t per_cta = 4 * kClusterWarps;
-  int64_t nc = (blocks + per_cta - 1) / per_cta;
-  if (nc > kMaxCluster) nc = kMaxCluster;
-  if (nc < 1) nc = 1;
-  const int64_t cb = (blocks + nc - 1) / nc;
-  nc = (blocks + cb - 1) / cb;
   // the warps' merge, then the CTA's partial o [G][hd] and (m, l) [G]
   size_t need = (size_t)kClusterWarps * G * (hd + 2) * sizeof(float);
   need = ((need + 15) & ~(size_t)15) + (size_t)G * hd * sizeof(float) + (size_t)G * 2 * sizeof(float);
   size_t smem = (size_t)kClusterWarps * ring + pre;
   if (smem < need) smem = need;
   if (smem > 200 * 1024) return false;
-  TcLaunchCfg q = *lc;
-  q.grid = dim3((unsigned)nc, c.n_kv_heads, batch);
-  q.smem = smem;
-  q.warps = kClusterWarps;
-  q.cluster = (int)nc;
+  int64_t hi = (blocks + kClusterWarps - 1) / kClusterWarps;   // one page per warp
+  if (hi > kMaxCluster) hi = kMaxCluster;
+  const int64_t lo = (blocks + kClusterWarps * max_ppw - 1) / (kClusterWarps * max_ppw);
   TcArgs none{};
-  if (max_active_clusters(fn, none, hd, nt, hd / c.k_group, q) < batch * c.n_kv_heads) return false;
-  *lc = q;
-  *cb_out = (int)cb;
-  return true;
+  for (int64_t want = hi; want >= lo && want >= 1; --want) {
+    const int64_t cb = (blocks + want - 1) / want;
+    const int64_t nc = (blocks + cb - 1) / cb;
+    if (nc != want) continue;   // the same split as a smaller cluster
+    TcLaunchCfg q = *lc;
+    q.grid = dim3((unsigned)nc, c.n_kv_heads, batch);
+    q.smem = smem;
+    q.warps = kClusterWarps;
+    q.cluster = (int)nc;
+    if (max_active_clusters(fn, none, hd, nt, hd / c.k_group, q) >= batch * c.n_kv_heads) {
+      *lc = q;
+      *cb_out = (int)cb;
+      return true;
+    }
+  }
+  return false;
 }
 
 // CTAs of the tensor-core kernel resident per SM (its launch bounds).

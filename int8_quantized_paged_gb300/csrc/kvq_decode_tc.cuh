@@ -91,9 +91,10 @@ __host__ __device__ constexpr int tc_qfrag_bytes(int hd, int nt) { return nt * h
 // Shared memory after the page rings: the query fragments, the RoPE row of
 // the query's position (hd / 2 cos/sin pairs), the affine-K per-group q sums
 // ([nt][ng][4 heads]) and, for a fused append, the new K and V rows (up to
-// fp32) with the RoPE row of their position.
+// fp32) with the RoPE row of their position, then their quantized rows (codes
+// up to 8-bit, parameter rows up to 64 bytes).
 __host__ __device__ constexpr int tc_pre_bytes(int hd, int nt, int ng) {
-  return tc_qfrag_bytes(hd, nt) + 4 * hd + 16 * nt * ng + 12 * hd;
+  return tc_qfrag_bytes(hd, nt) + 4 * hd + 16 * nt * ng + 14 * hd + 128;
 }
 
 // Fused append: quantizes the staged row (K rotated at its position) exactly
@@ -389,8 +390,12 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       asm volatile("cp.async.commit_group;" ::: "memory");
     }
   }
-  // Quantizes the staged rows into the pool and, for s >= 0, into slot s.
-  auto write_app = [&](int s) {
+  // The quantized rows, in the pool's row format, after the staged rows:
+  // K codes [KRB], V codes [VRB], K parameter row, V parameter row.
+  const int qk_off = app_off + 12 * HD, qv_off = qk_off + KRB, qkp_off = qv_off + VRB, qvp_off = qkp_off + 64;
+  // Quantizes the staged rows (their copies have landed) into the pool and
+  // into the row buffers above.
+  auto quantize_app = [&]() {
     const uint8_t* st = smem + app_off;
     const float2* cs = a.rope != KVQ_ROPE_NONE ? reinterpret_cast<const float2*>(st + 8 * HD) : nullptr;
     const int r = apos % P;
@@ -400,22 +405,32 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
               r, lane);
     store_row(vq, a.vl, const_cast<uint8_t*>(a.v_pool) + (int64_t)app_pg * a.vl.page_bytes + (int64_t)kvh * a.vl.sub_bytes,
               r, lane);
-    if (s >= 0) {
-      uint8_t* slot = smem + (w * D + s) * SLOT;
-      const int jk = lane * kq.nbytes, jv = lane * vq.nbytes;
-      store_code_bytes(slot + swz<KRB>(r, jk / 16) + jk % 16, kq.w, kq.nbytes);
-      store_code_bytes(slot + KC + swz<VRB>(r, jv / 16) + jv % 16, vq.w, vq.nbytes);
-      uint8_t* kpr = slot + KC + VC + r * a.kl.param_row_bytes;
-      uint8_t* vpr = slot + KC + VC + KPMAX + r * a.vl.param_row_bytes;
-      if (kq.leader) {
-        store_param(kpr + param_scale_offset(a.kl, kq.group), a.kl.param, kq.scale);
-        if (KAFF) store_param(kpr + param_bias_offset(a.kl, kq.group), a.kl.param, kq.bias);
-      }
-      if (vq.leader) {
-        store_param(vpr + param_scale_offset(a.vl, vq.group), a.vl.param, vq.scale);
-        if (VAFF) store_param(vpr + param_bias_offset(a.vl, vq.group), a.vl.param, vq.bias);
-      }
+    store_code_bytes(smem + qk_off + lane * kq.nbytes, kq.w, kq.nbytes);
+    store_code_bytes(smem + qv_off + lane * vq.nbytes, vq.w, vq.nbytes);
+    if (kq.leader) {
+      store_param(smem + qkp_off + param_scale_offset(a.kl, kq.group), a.kl.param, kq.scale);
+      if (KAFF) store_param(smem + qkp_off + param_bias_offset(a.kl, kq.group), a.kl.param, kq.bias);
     }
+    if (vq.leader) {
+      store_param(smem + qvp_off + param_scale_offset(a.vl, vq.group), a.vl.param, vq.scale);
+      if (VAFF) store_param(smem + qvp_off + param_bias_offset(a.vl, vq.group), a.vl.param, vq.bias);
+    }
+  };
+  // Writes the quantized rows over row apos % P of slot s (codes swizzled
+  // like the page copies).
+  auto place_app = [&](int s) {
+    uint8_t* slot = smem + (w * D + s) * SLOT;
+    const int r = apos % P;
+    if (lane < KCH) {
+      const uint4 x = *reinterpret_cast<const uint4*>(smem + qk_off + 16 * lane);
+      *reinterpret_cast<uint4*>(slot + swz<KRB>(r, lane)) = x;
+    } else if (lane >= 16 && lane - 16 < VCH) {
+      const uint4 x = *reinterpret_cast<const uint4*>(smem + qv_off + 16 * (lane - 16));
+      *reinterpret_cast<uint4*>(slot + KC + swz<VRB>(r, lane - 16)) = x;
+    }
+    const int kprb_ = a.kl.param_row_bytes, vprb_ = a.vl.param_row_bytes;
+    for (int j = lane; j < kprb_; j += 32) slot[KC + VC + r * kprb_ + j] = smem[qkp_off + j];
+    for (int j = lane; j < vprb_; j += 32) slot[KC + VC + KPMAX + r * vprb_ + j] = smem[qvp_off + j];
   };
 
   uint32_t valid = 0;   // bit s: slot s holds a page
@@ -534,7 +549,13 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       }
     }
   }
-  if (k_app == -2) write_app(-1);   // warp 0, past its wait for the staged rows above
+  // The new row is quantized now, while the warp's pages are still arriving.
+  if (k_app != -1) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(D) : "memory");   // the staged rows: older than the pages
+    __syncwarp();
+    quantize_app();
+    __syncwarp();
+  }
   __syncthreads();
   // affine K: the q sums of this lane's score head 4nt + tig (mod G)
   float qsum[NT][KNG];
@@ -593,8 +614,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     // and the warp's lanes see each other's copies after the sync
     asm volatile("cp.async.wait_group %0;" ::"n"(D - 1) : "memory");
     __syncwarp();
-    if (k == k_app) {   // the new row's page (its staged rows landed before it)
-      write_app(s);
+    if (k == k_app) {   // the new row's page: its stale copy of the row is replaced
+      place_app(s);
       __syncwarp();
     }
     if ((valid >> s) & 1u) {
