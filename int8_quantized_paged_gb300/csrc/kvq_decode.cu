@@ -109,10 +109,10 @@ static size_t tc_ring_bytes(const kvq_config& c) {
 }
 
 // The cluster mode: a few sequences, each short enough that one cluster of
-// up to kMaxCluster CTAs of kClusterWarps warps covers it with at most eight
-// pages per warp, and all the clusters resident at once.  The cluster is as
-// large as that allows, down to one page per warp: the pages of a short
-// context spread over as many SMs as possible.  On success fills the launch
+// up to kMaxCluster CTAs of kClusterWarps warps (one CTA per SM) covers it
+// with at most eight pages per warp, and all the clusters resident at once.
+// The cluster is as large as that allows, down to one page per warp: the
+// pages of a short context spread over as many SMs as possible.  On success fills the launch
 // configuration (grid, shared memory, warps, cluster size) and the 16-token
 // blocks per CTA.
 static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens, int32_t window, TcLaunch fn,
@@ -131,6 +131,11 @@ static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens,
   need = ((need + 15) & ~(size_t)15) + (size_t)G * hd * sizeof(float) + (size_t)G * 2 * sizeof(float);
   size_t smem = (size_t)kClusterWarps * ring + pre;
   if (smem < need) smem = need;
+  // One CTA per SM: with two, some SMs hold two CTAs of a cluster while others
+  // idle, and those CTAs finish last (measured: a smaller cluster at one CTA
+  // per SM is faster than 16 CTAs placed two to an SM).
+  if (smem < smem_per_sm() / 2 + 1) smem = smem_per_sm() / 2 + 1;
+  smem = (smem + 15) & ~(size_t)15;
   if (smem > 200 * 1024) return false;
   int64_t hi = (blocks + kClusterWarps - 1) / kClusterWarps;   // one page per warp
   if (hi > kMaxCluster) hi = kMaxCluster;

@@ -84,7 +84,7 @@ __host__ __device__ constexpr int tc_min_blocks(int hd, int nt) { return hd <= 1
 // Shapes with a cluster-mode instantiation (one 8-column tile: G <= 4), and
 // the cluster-mode CTAs resident per SM.
 __host__ __device__ constexpr bool tc_cluster_shape(int hd, int nt) { return nt == 1; }
-__host__ __device__ constexpr int tc_cluster_min_blocks(int hd) { return hd <= 128 ? 2 : 1; }
+__host__ __device__ constexpr int tc_cluster_min_blocks(int hd) { return 1; }
 // Shared memory of the query fragments (the same for every warp of a CTA):
 // NT tiles x hd/16 k-steps x 2 words x 32 lanes.
 __host__ __device__ constexpr int tc_qfrag_bytes(int hd, int nt) { return nt * hd * 16; }
@@ -300,8 +300,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   const uint32_t wring = tc::smem_u32(smem) + (uint32_t)(w * D * SLOT);
   const bool vlane = lane >= 16;
   const int hl = lane & 15;
-  const int n_sub = vlane ? (VC + A.vp_bytes) / 16 : (KC + A.kp_bytes) / 16;   // chunks of the sub-block
-  const int cnt = n_sub > hl ? (n_sub - hl + 15) / 16 : 0;                     // this lane's copies
+  constexpr int KSUB = (KC + KPMAX) / 16, VSUB = (VC + VPMAX) / 16;   // 16-byte chunks of a sub-block
+  constexpr int NCP_ALL = cmin(KSUB, VSUB) / 16;                       // copies every lane makes
+  const int n_sub = vlane ? VSUB : KSUB;
+  const int cnt = n_sub > hl ? (n_sub - hl + 15) / 16 : 0;             // this lane's copies
   uint32_t cp_dst[NCP];
 #pragma unroll
   for (int m = 0; m < NCP; ++m) {
@@ -428,7 +430,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       const uint4 x = *reinterpret_cast<const uint4*>(smem + qv_off + 16 * (lane - 16));
       *reinterpret_cast<uint4*>(slot + KC + swz<VRB>(r, lane - 16)) = x;
     }
-    const int kprb_ = a.kl.param_row_bytes, vprb_ = a.vl.param_row_bytes;
+    constexpr int kprb_ = NG * (KAFF ? 2 : 1) * PB, vprb_ = NG * (VAFF ? 2 : 1) * PB;
     for (int j = lane; j < kprb_; j += 32) slot[KC + VC + r * kprb_ + j] = smem[qkp_off + j];
     for (int j = lane; j < vprb_; j += 32) slot[KC + VC + KPMAX + r * vprb_ + j] = smem[qvp_off + j];
   };
@@ -440,10 +442,11 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     valid = pg >= 0 ? (valid | (1u << s)) : (valid & ~(1u << s));
     if (pg < 0) return;
     const uint8_t* src = pool_lane + pg * page_lane;
+    const uint32_t so = s * SLOT;
 #pragma unroll
     for (int m = 0; m < NCP; ++m)
-      if (m < cnt)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(cp_dst[m] + s * SLOT), "l"(src + 256 * m)
+      if (m < NCP_ALL || m < cnt)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(cp_dst[m] + so), "l"(src + 256 * m)
                      : "memory");
   };
 #pragma unroll
@@ -572,8 +575,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     }
 
   // ---- per-lane constants of the main loop
-  const int kprb = a.kl.param_row_bytes, vprb = a.vl.param_row_bytes;
-  const int kstep = a.kl.n_params * PB, vstep = a.vl.n_params * PB;   // bytes per group in a param row
+  // parameter rows: per group a scale (and an affine bias) of PB bytes; the
+  // host checks that the pools' rows have this layout
+  constexpr int kstep = (KAFF ? 2 : 1) * PB, vstep = (VAFF ? 2 : 1) * PB;   // bytes per group in a row
+  constexpr int kprb = NG * kstep, vprb = NG * vstep;                        // bytes per row
   const int mi = lane >> 3;
   const int trow = 8 * (mi & 1) + (lane & 7);    // token row this lane addresses in ldmatrix
   int kls[KCH / 2], vls[VCH / 2];

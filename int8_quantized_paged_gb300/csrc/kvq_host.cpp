@@ -112,6 +112,19 @@ float score_scale_log2(const kvq_config& c) {
   return (float)(alpha * 1.4426950408889634);  // log2(e)
 }
 
+size_t smem_per_sm() {
+  static size_t cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 228 * 1024;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || n <= 0)
+      n = 228 * 1024;
+    cache[dev] = (size_t)n;
+  }
+  return cache[dev];
+}
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;

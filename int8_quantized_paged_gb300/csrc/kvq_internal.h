@@ -48,6 +48,7 @@ float score_scale_log2(const kvq_config& c);
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
+size_t smem_per_sm();   // shared memory of one SM of the current device (bytes)
 
 // Whether kernels are launched with programmatic dependent launch (set
 // KVQ_PDL=0 in the environment to turn it off).

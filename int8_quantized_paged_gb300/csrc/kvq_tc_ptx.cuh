@@ -244,53 +244,51 @@ __device__ __forceinline__ void q8_codes(uint32_t x, uint32_t (&h)[2]) {
 // word each, 8 nibbles).  k-step "even" uses nibbles (0,4 | 2,6), "odd" uses
 // (1,5 | 3,7); B fragments be / bo; D += A * B.
 #define KVQ_Q4_PRE(K0, K1, X0, X8)                                        \
-  " .reg .b32 u0, u1, t, a0, a1, a2, a3, e0, e1, e2, e3, k0, k1;\n"      \
-  " mov.b32 k0, " K0 ";\n mov.b32 k1, " K1 ";\n"                         \
+  " .reg .b32 u0, u1, t, a0, a1, a2, a3, e0, e1, e2, e3;\n"              \
   " shr.b32 u0, " X0 ", 8;\n shr.b32 u1, " X8 ", 8;\n"                   \
-  " lop3.b32 t, " X0 ", 0x000F000F, k0, 0x6a;\n sub.rn.f16x2 a0, t, k0;\n" \
-  " lop3.b32 t, " X8 ", 0x000F000F, k0, 0x6a;\n sub.rn.f16x2 a1, t, k0;\n" \
-  " lop3.b32 t, u0, 0x000F000F, k0, 0x6a;\n sub.rn.f16x2 a2, t, k0;\n"   \
-  " lop3.b32 t, u1, 0x000F000F, k0, 0x6a;\n sub.rn.f16x2 a3, t, k0;\n"   \
-  " lop3.b32 t, " X0 ", 0x00F000F0, k1, 0x6a;\n sub.rn.f16x2 e0, t, k1;\n" \
-  " lop3.b32 t, " X8 ", 0x00F000F0, k1, 0x6a;\n sub.rn.f16x2 e1, t, k1;\n" \
-  " lop3.b32 t, u0, 0x00F000F0, k1, 0x6a;\n sub.rn.f16x2 e2, t, k1;\n"   \
-  " lop3.b32 t, u1, 0x00F000F0, k1, 0x6a;\n sub.rn.f16x2 e3, t, k1;\n"
+  " lop3.b32 t, " X0 ", 0x000F000F, " K0 ", 0x6a;\n sub.rn.f16x2 a0, t, " K0 ";\n" \
+  " lop3.b32 t, " X8 ", 0x000F000F, " K0 ", 0x6a;\n sub.rn.f16x2 a1, t, " K0 ";\n" \
+  " lop3.b32 t, u0, 0x000F000F, " K0 ", 0x6a;\n sub.rn.f16x2 a2, t, " K0 ";\n"   \
+  " lop3.b32 t, u1, 0x000F000F, " K0 ", 0x6a;\n sub.rn.f16x2 a3, t, " K0 ";\n"   \
+  " lop3.b32 t, " X0 ", 0x00F000F0, " K1 ", 0x6a;\n sub.rn.f16x2 e0, t, " K1 ";\n" \
+  " lop3.b32 t, " X8 ", 0x00F000F0, " K1 ", 0x6a;\n sub.rn.f16x2 e1, t, " K1 ";\n" \
+  " lop3.b32 t, u0, 0x00F000F0, " K1 ", 0x6a;\n sub.rn.f16x2 e2, t, " K1 ";\n"   \
+  " lop3.b32 t, u1, 0x00F000F0, " K1 ", 0x6a;\n sub.rn.f16x2 e3, t, " K1 ";\n"
 #define KVQ_MMA(D, A0, A1, A2, A3, B0, B1)                                                       \
   " mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {" D "}, {" A0 "," A1 "," A2 "," A3 "}, {" B0 \
   "," B1 "}, {" D "};\n"
 // lop3 immediate 0x6a = (a & b) ^ c.  Symmetric nibbles: offsets 8 (bits 0..3)
 // and 0x80 (bits 4..7), i.e. n + 8 and 16 * (n + 8) in the mantissa of 1024;
 // affine nibbles: no offset.
-#define KVQ_S4 "0x64086408", "0x64806480"
-#define KVQ_A4 "0x64006400", "0x64006400"
+// The two constants are register operands: the caller's loop holds them in
+// registers instead of every block materializing them.
+template <bool AFF>
+__device__ __forceinline__ uint32_t q4_magic_lo() { return AFF ? 0x64006400u : 0x64086408u; }
+template <bool AFF>
+__device__ __forceinline__ uint32_t q4_magic_hi() { return AFF ? 0x64006400u : 0x64806480u; }
 
 // Q.K, 4-bit K, one 8-column tile: 2 MMAs into d.
 template <bool AFF>
 __device__ __forceinline__ void qk4(uint32_t x0, uint32_t x8, const uint32_t (&be)[2], const uint32_t (&bo)[2],
                                     float (&d)[4]) {
-#define KVQ_BODY(OFF)                                                                               \
-  asm volatile("{\n" KVQ_Q4_PRE(OFF, "%4", "%5") KVQ_MMA("%0,%1,%2,%3", "a0", "a1", "a2", "a3", "%6", "%7") \
-               KVQ_MMA("%0,%1,%2,%3", "e0", "e1", "e2", "e3", "%8", "%9") "}\n"                     \
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])                                      \
-               : "r"(x0), "r"(x8), "r"(be[0]), "r"(be[1]), "r"(bo[0]), "r"(bo[1]))
-  if constexpr (AFF) KVQ_BODY(KVQ_A4); else KVQ_BODY(KVQ_S4);
-#undef KVQ_BODY
+  asm volatile("{\n" KVQ_Q4_PRE("%10", "%11", "%4", "%5") KVQ_MMA("%0,%1,%2,%3", "a0", "a1", "a2", "a3", "%6", "%7")
+               KVQ_MMA("%0,%1,%2,%3", "e0", "e1", "e2", "e3", "%8", "%9") "}\n"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(x0), "r"(x8), "r"(be[0]), "r"(be[1]), "r"(bo[0]), "r"(bo[1]), "r"(q4_magic_lo<AFF>()),
+                 "r"(q4_magic_hi<AFF>()));
 }
 
 // Q.K, 4-bit K, two 8-column tiles: 4 MMAs into d / f.
 template <bool AFF>
 __device__ __forceinline__ void qk4x2(uint32_t x0, uint32_t x8, const uint32_t (&be)[2], const uint32_t (&bo)[2],
                                       const uint32_t (&ce)[2], const uint32_t (&co)[2], float (&d)[4], float (&f)[4]) {
-#define KVQ_BODY(OFF)                                                                                 \
-  asm volatile("{\n" KVQ_Q4_PRE(OFF, "%8", "%9") KVQ_MMA("%0,%1,%2,%3", "a0", "a1", "a2", "a3", "%10", "%11") \
-               KVQ_MMA("%0,%1,%2,%3", "e0", "e1", "e2", "e3", "%12", "%13")                           \
-               KVQ_MMA("%4,%5,%6,%7", "a0", "a1", "a2", "a3", "%14", "%15")                           \
-               KVQ_MMA("%4,%5,%6,%7", "e0", "e1", "e2", "e3", "%16", "%17") "}\n"                     \
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3]), "+f"(f[0]), "+f"(f[1]), "+f"(f[2]), "+f"(f[3]) \
-               : "r"(x0), "r"(x8), "r"(be[0]), "r"(be[1]), "r"(bo[0]), "r"(bo[1]), "r"(ce[0]), "r"(ce[1]),   \
-                 "r"(co[0]), "r"(co[1]))
-  if constexpr (AFF) KVQ_BODY(KVQ_A4); else KVQ_BODY(KVQ_S4);
-#undef KVQ_BODY
+  asm volatile("{\n" KVQ_Q4_PRE("%18", "%19", "%8", "%9") KVQ_MMA("%0,%1,%2,%3", "a0", "a1", "a2", "a3", "%10", "%11")
+               KVQ_MMA("%0,%1,%2,%3", "e0", "e1", "e2", "e3", "%12", "%13")
+               KVQ_MMA("%4,%5,%6,%7", "a0", "a1", "a2", "a3", "%14", "%15")
+               KVQ_MMA("%4,%5,%6,%7", "e0", "e1", "e2", "e3", "%16", "%17") "}\n"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3]), "+f"(f[0]), "+f"(f[1]), "+f"(f[2]), "+f"(f[3])
+               : "r"(x0), "r"(x8), "r"(be[0]), "r"(be[1]), "r"(bo[0]), "r"(bo[1]), "r"(ce[0]), "r"(ce[1]),
+                 "r"(co[0]), "r"(co[1]), "r"(q4_magic_lo<AFF>()), "r"(q4_magic_hi<AFF>()));
 }
 
 // P.V, 4-bit V (A = V^T from ldmatrix.trans): y0 = the tokens 0-7 word, y8 =
@@ -299,62 +297,58 @@ __device__ __forceinline__ void qk4x2(uint32_t x0, uint32_t x8, const uint32_t (
 // the odd one (16 x code, rows 4g+1, 4g+3) A = {e0, e2, e1, e3}.
 template <bool AFF>
 __device__ __forceinline__ void pv4(uint32_t y0, uint32_t y8, const uint32_t (&b)[2], float (&de)[4], float (&dodd)[4]) {
-#define KVQ_BODY(OFF)                                                                               \
-  asm volatile("{\n" KVQ_Q4_PRE(OFF, "%8", "%9") KVQ_MMA("%0,%1,%2,%3", "a0", "a2", "a1", "a3", "%10", "%11") \
-               KVQ_MMA("%4,%5,%6,%7", "e0", "e2", "e1", "e3", "%10", "%11") "}\n"                   \
-               : "+f"(de[0]), "+f"(de[1]), "+f"(de[2]), "+f"(de[3]), "+f"(dodd[0]), "+f"(dodd[1]),   \
-                 "+f"(dodd[2]), "+f"(dodd[3])                                                         \
-               : "r"(y0), "r"(y8), "r"(b[0]), "r"(b[1]))
-  if constexpr (AFF) KVQ_BODY(KVQ_A4); else KVQ_BODY(KVQ_S4);
-#undef KVQ_BODY
+  asm volatile("{\n" KVQ_Q4_PRE("%12", "%13", "%8", "%9") KVQ_MMA("%0,%1,%2,%3", "a0", "a2", "a1", "a3", "%10", "%11")
+               KVQ_MMA("%4,%5,%6,%7", "e0", "e2", "e1", "e3", "%10", "%11") "}\n"
+               : "+f"(de[0]), "+f"(de[1]), "+f"(de[2]), "+f"(de[3]), "+f"(dodd[0]), "+f"(dodd[1]),
+                 "+f"(dodd[2]), "+f"(dodd[3])
+               : "r"(y0), "r"(y8), "r"(b[0]), "r"(b[1]), "r"(q4_magic_lo<AFF>()), "r"(q4_magic_hi<AFF>()));
 }
 
 // P.V, 4-bit V, two 8-column tiles (weights b for tile 0, c for tile 1).
 template <bool AFF>
 __device__ __forceinline__ void pv4x2(uint32_t y0, uint32_t y8, const uint32_t (&b)[2], const uint32_t (&c)[2],
                                       float (&de)[4], float (&dodd)[4], float (&fe)[4], float (&fodd)[4]) {
-#define KVQ_BODY(OFF)                                                                                 \
-  asm volatile("{\n" KVQ_Q4_PRE(OFF, "%16", "%17")                                                    \
-               KVQ_MMA("%0,%1,%2,%3", "a0", "a2", "a1", "a3", "%18", "%19")                           \
-               KVQ_MMA("%4,%5,%6,%7", "e0", "e2", "e1", "e3", "%18", "%19")                           \
-               KVQ_MMA("%8,%9,%10,%11", "a0", "a2", "a1", "a3", "%20", "%21")                         \
-               KVQ_MMA("%12,%13,%14,%15", "e0", "e2", "e1", "e3", "%20", "%21") "}\n"                 \
-               : "+f"(de[0]), "+f"(de[1]), "+f"(de[2]), "+f"(de[3]), "+f"(dodd[0]), "+f"(dodd[1]),     \
-                 "+f"(dodd[2]), "+f"(dodd[3]), "+f"(fe[0]), "+f"(fe[1]), "+f"(fe[2]), "+f"(fe[3]),       \
-                 "+f"(fodd[0]), "+f"(fodd[1]), "+f"(fodd[2]), "+f"(fodd[3])                             \
-               : "r"(y0), "r"(y8), "r"(b[0]), "r"(b[1]), "r"(c[0]), "r"(c[1]))
-  if constexpr (AFF) KVQ_BODY(KVQ_A4); else KVQ_BODY(KVQ_S4);
-#undef KVQ_BODY
+  asm volatile("{\n" KVQ_Q4_PRE("%22", "%23", "%16", "%17")
+               KVQ_MMA("%0,%1,%2,%3", "a0", "a2", "a1", "a3", "%18", "%19")
+               KVQ_MMA("%4,%5,%6,%7", "e0", "e2", "e1", "e3", "%18", "%19")
+               KVQ_MMA("%8,%9,%10,%11", "a0", "a2", "a1", "a3", "%20", "%21")
+               KVQ_MMA("%12,%13,%14,%15", "e0", "e2", "e1", "e3", "%20", "%21") "}\n"
+               : "+f"(de[0]), "+f"(de[1]), "+f"(de[2]), "+f"(de[3]), "+f"(dodd[0]), "+f"(dodd[1]),
+                 "+f"(dodd[2]), "+f"(dodd[3]), "+f"(fe[0]), "+f"(fe[1]), "+f"(fe[2]), "+f"(fe[3]),
+                 "+f"(fodd[0]), "+f"(fodd[1]), "+f"(fodd[2]), "+f"(fodd[3])
+               : "r"(y0), "r"(y8), "r"(b[0]), "r"(b[1]), "r"(c[0]), "r"(c[1]), "r"(q4_magic_lo<AFF>()),
+                 "r"(q4_magic_hi<AFF>()));
 }
 
 // 8-bit codes: x = bytes b0..b3 -> (b0, b2) and (b1, b3) as fp16 (XOR 0x80,
 // mantissa of 1024, minus 1152).
-#define KVQ_Q8_PRE(X0, X8)                                                   \
-  " .reg .b32 u0, u1, t, a0, a1, a2, a3, k0;\n mov.b32 k0, 0x64806480;\n"     \
+#define KVQ_Q8_PRE(K0, X0, X8)                                               \
+  " .reg .b32 u0, u1, t, a0, a1, a2, a3;\n"                                  \
   " shr.b32 u0, " X0 ", 8;\n shr.b32 u1, " X8 ", 8;\n"                       \
-  " lop3.b32 t, " X0 ", 0x00FF00FF, k0, 0x6a;\n sub.rn.f16x2 a0, t, k0;\n"   \
-  " lop3.b32 t, " X8 ", 0x00FF00FF, k0, 0x6a;\n sub.rn.f16x2 a1, t, k0;\n"   \
-  " lop3.b32 t, u0, 0x00FF00FF, k0, 0x6a;\n sub.rn.f16x2 a2, t, k0;\n"       \
-  " lop3.b32 t, u1, 0x00FF00FF, k0, 0x6a;\n sub.rn.f16x2 a3, t, k0;\n"
+  " lop3.b32 t, " X0 ", 0x00FF00FF, " K0 ", 0x6a;\n sub.rn.f16x2 a0, t, " K0 ";\n" \
+  " lop3.b32 t, " X8 ", 0x00FF00FF, " K0 ", 0x6a;\n sub.rn.f16x2 a1, t, " K0 ";\n" \
+  " lop3.b32 t, u0, 0x00FF00FF, " K0 ", 0x6a;\n sub.rn.f16x2 a2, t, " K0 ";\n"     \
+  " lop3.b32 t, u1, 0x00FF00FF, " K0 ", 0x6a;\n sub.rn.f16x2 a3, t, " K0 ";\n"
+constexpr uint32_t kQ8Magic = 0x64806480u;
 
 // Q.K, 8-bit K: A = {x0.(b0,b2), x8.(b0,b2), x0.(b1,b3), x8.(b1,b3)}; one or two tiles.
 __device__ __forceinline__ void qk8(uint32_t x0, uint32_t x8, const uint32_t (&b)[2], float (&d)[4]) {
-  asm volatile("{\n" KVQ_Q8_PRE("%4", "%5") KVQ_MMA("%0,%1,%2,%3", "a0", "a1", "a2", "a3", "%6", "%7") "}\n"
+  asm volatile("{\n" KVQ_Q8_PRE("%8", "%4", "%5") KVQ_MMA("%0,%1,%2,%3", "a0", "a1", "a2", "a3", "%6", "%7") "}\n"
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(x0), "r"(x8), "r"(b[0]), "r"(b[1]));
+               : "r"(x0), "r"(x8), "r"(b[0]), "r"(b[1]), "r"(kQ8Magic));
 }
 __device__ __forceinline__ void qk8x2(uint32_t x0, uint32_t x8, const uint32_t (&b)[2], const uint32_t (&c)[2],
                                       float (&d)[4], float (&f)[4]) {
-  asm volatile("{\n" KVQ_Q8_PRE("%8", "%9") KVQ_MMA("%0,%1,%2,%3", "a0", "a1", "a2", "a3", "%10", "%11")
+  asm volatile("{\n" KVQ_Q8_PRE("%14", "%8", "%9") KVQ_MMA("%0,%1,%2,%3", "a0", "a1", "a2", "a3", "%10", "%11")
                KVQ_MMA("%4,%5,%6,%7", "a0", "a1", "a2", "a3", "%12", "%13") "}\n"
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3]), "+f"(f[0]), "+f"(f[1]), "+f"(f[2]), "+f"(f[3])
-               : "r"(x0), "r"(x8), "r"(b[0]), "r"(b[1]), "r"(c[0]), "r"(c[1]));
+               : "r"(x0), "r"(x8), "r"(b[0]), "r"(b[1]), "r"(c[0]), "r"(c[1]), "r"(kQ8Magic));
 }
 // P.V, 8-bit V: A = {y0.(b0,b2), y0.(b1,b3), y8.(b0,b2), y8.(b1,b3)}.
 __device__ __forceinline__ void pv8(uint32_t y0, uint32_t y8, const uint32_t (&b)[2], float (&d)[4]) {
-  asm volatile("{\n" KVQ_Q8_PRE("%4", "%5") KVQ_MMA("%0,%1,%2,%3", "a0", "a2", "a1", "a3", "%6", "%7") "}\n"
+  asm volatile("{\n" KVQ_Q8_PRE("%8", "%4", "%5") KVQ_MMA("%0,%1,%2,%3", "a0", "a2", "a1", "a3", "%6", "%7") "}\n"
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(y0), "r"(y8), "r"(b[0]), "r"(b[1]));
+               : "r"(y0), "r"(y8), "r"(b[0]), "r"(b[1]), "r"(kQ8Magic));
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
