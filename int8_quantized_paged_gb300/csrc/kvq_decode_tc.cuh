@@ -611,10 +611,289 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 #pragma unroll
   for (int g = 0; g < VNG; ++g) vinv[g] = 0.f;
 
+  // ---- one page (16 tokens) of a slot: its scores, then its P.V.
+  // Q.K of the page in slot sl, whose row 0 is absolute token tb.
+  auto page_scores = [&](int sl, int tb, bool edge, float (&sc)[NT][2]) {
+    const uint32_t kc = wring + sl * SLOT;
+    const uint32_t kp = kc + KC + VC;
+    // ---- Q.K: A = codes of tokens (gid, gid+8), B = q fragments
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = 0.f;
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+    // fold the accumulated dots of K group g into the scores
+    auto fold = [&](int g) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t pr = kp + (gid + 8 * j) * kprb + g * kstep;
+        const float ks = ld_param<PT>(pr) * (1.0f / kQScale);
+        float kb = 0.f;
+        if constexpr (KAFF) kb = ld_param<PT>(pr + PB);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float v = ks * fmaf(sacc[nt][2 * j + 1], 1.0f / tc::kLoScale, sacc[nt][2 * j]);
+          if constexpr (KAFF) {
+            float qs = qsum[nt][0];
+#pragma unroll
+            for (int gg = 1; gg < KNG; ++gg)
+              if (gg == g) qs = qsum[nt][gg];
+            v = fmaf(kb, qs, v);
+          }
+          sc[nt][j] += v;
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+    };
+#pragma unroll
+    for (int c2 = 0; c2 < KCH / 2; ++c2) {
+      uint32_t r[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
+      tc::ldsm_x4(kc + kls[c2], r);
+      // query fragments of chunks 2c2, 2c2+1: uint4s (K8: one for both, 4-bit: one each)
+      uint32_t qf[NT][2][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int cc = 0; cc < (K8 ? 1 : 2); ++cc) {
+          const int i = K8 ? c2 : 2 * c2 + cc;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(qf[nt][cc][0]), "=r"(qf[nt][cc][1]), "=r"(qf[nt][cc][2]), "=r"(qf[nt][cc][3])
+                       : "r"(qfs + ((nt * (KSTEPS / 2) + i) * 32 + lane) * 16));
+        }
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * c2 + cc;
+        // codes of tokens gid / gid+8 -> fp16 fragments -> MMAs, in one PTX block
+        if constexpr (K8) {   // k-step c: words 2cc, 2cc+1 of the uint4
+          const uint32_t b0[2] = {qf[0][0][2 * cc], qf[0][0][2 * cc + 1]};
+          if constexpr (NT == 1) {
+            tc::qk8(r[2 * cc], r[2 * cc + 1], b0, sacc[0]);
+          } else {
+            const uint32_t b1[2] = {qf[1][0][2 * cc], qf[1][0][2 * cc + 1]};
+            tc::qk8x2(r[2 * cc], r[2 * cc + 1], b0, b1, sacc[0], sacc[1]);
+          }
+        } else {              // k-steps 2c, 2c+1: the uint4 of chunk c
+          const uint32_t be0[2] = {qf[0][cc][0], qf[0][cc][1]}, bo0[2] = {qf[0][cc][2], qf[0][cc][3]};
+          if constexpr (NT == 1) {
+            tc::qk4<KAFF>(r[2 * cc], r[2 * cc + 1], be0, bo0, sacc[0]);
+          } else {
+            const uint32_t be1[2] = {qf[1][cc][0], qf[1][cc][1]}, bo1[2] = {qf[1][cc][2], qf[1][cc][3]};
+            tc::qk4x2<KAFF>(r[2 * cc], r[2 * cc + 1], be0, bo0, be1, bo1, sacc[0], sacc[1]);
+          }
+        }
+        if constexpr (!ONEG) {
+          if ((KDC * (c + 1)) % GS == 0) fold((KDC * c) / GS);
+        }
+      }
+    }
+    if constexpr (ONEG) fold(0);
+    if (edge) {   // the page at the window start or the context end
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int t = tb + gid + 8 * j;
+        if (t < lo || t >= L)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) sc[nt][j] = -INFINITY;
+      }
+    }
+
+  };
+  // The running max, raised (lazily) when this lane's scores bm pass it.
+  auto raise_max = [&](const float (&bm)[NT]) {
+    bool raise = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) raise |= bm[nt] > m[nt] + kLazyMax;
+    if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float x = bm[nt];
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
+        if (x > m[nt] + kLazyMax) {
+          const float corr = m[nt] == -INFINITY ? 0.f : tc::ex2(m[nt] - x);
+          l[nt] *= corr;
+#pragma unroll
+          for (int g = 0; g < VNG; ++g) pbias[nt][g] *= corr;
+#pragma unroll
+          for (int t = 0; t < MT; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[t][nt][e] *= corr;
+          m[nt] = x;
+        }
+      }
+    }
+  };
+  // p = 2^(s - m) (0 for masked tokens, s = -inf), added to l.
+  auto probs = [&](const float (&sc)[NT][2], float (&p)[NT][2]) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float mu = m[nt] == -INFINITY ? 0.f : m[nt];
+      p[nt][0] = tc::ex2(sc[nt][0] - mu);
+      p[nt][1] = tc::ex2(sc[nt][1] - mu);
+      l[nt] += p[nt][0] + p[nt][1];
+    }
+  };
+  // P.V of the page in slot sl with probabilities p.
+  auto page_pv = [&](int sl, int tb, bool edge, const float (&p)[NT][2]) {
+    const uint32_t vc = wring + sl * SLOT + KC;
+    const uint32_t vp = wring + sl * SLOT + KC + VC + KPMAX;
+    // ---- P.V: A = V^T codes (ldmatrix.trans), B = weights of V group g.
+    // Entering group g: its scales for the lane's tokens (gid, gid+8), a
+    // raise of its reference when a scale passes half of it (2x headroom),
+    // then w = p * scale * vinv formed here and moved to the B layout.
+    uint32_t bw[NT][2];
+    auto weights = [&](int g) {
+      float vs[2], vb[2] = {0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t pr = vp + (gid + 8 * j) * vprb + g * vstep;
+        vs[j] = ld_param<PT>(pr);
+        if constexpr (VAFF) vb[j] = ld_param<PT>(pr + PB);
+        if (edge) {
+          const int t = tb + gid + 8 * j;
+          if (t < lo || t >= L) vs[j] = vb[j] = 0.f;
+        }
+      }
+      float vig = vinv[0];
+#pragma unroll
+      for (int gg = 1; gg < VNG; ++gg)
+        if (gg == g) vig = vinv[gg];
+      // a scale above half the reference: 2 * scale * vinv > kWScale
+      if (__any_sync(0xffffffffu, 2.0f * fmaxf(vs[0], vs[1]) * vig > kWScale || vig == 0.f)) {
+        float sm = fmaxf(vs[0], vs[1]);
+        sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 4));
+        sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 8));
+        sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 16));
+        if (sm > 0.f && (vig == 0.f || 2.0f * sm * vig > kWScale)) {
+          const float nvi = kWScale / (2.0f * sm);
+          if (vig > 0.f) {
+            const float ratio = nvi / vig;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+              const int c = V8 ? t : (t >> 1);
+              if ((VDC * c) / GS == g)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) oacc[t][nt][e] *= ratio;
+            }
+          }
+          vig = nvi;
+#pragma unroll
+          for (int gg = 0; gg < VNG; ++gg)
+            if (gg == g) vinv[gg] = nvi;
+        }
+      }
+      if constexpr (VAFF) {
+#pragma unroll
+        for (int gg = 0; gg < VNG; ++gg)
+          if (gg == g)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              pbias[nt][gg] = fmaf(p[nt][0], vb[0], fmaf(p[nt][1], vb[1], pbias[nt][gg]));
+      }
+      const float w0 = vs[0] * vig, w1 = vs[1] * vig;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t r0 = hilo_pack(p[nt][0] * w0);   // token gid
+        const uint32_t r1 = hilo_pack(p[nt][1] * w1);   // token gid + 8
+        const uint32_t u00 = __shfl_sync(0xffffffffu, r0, src0);  // token 2tig
+        const uint32_t u10 = __shfl_sync(0xffffffffu, r0, src1);  // token 2tig + 1
+        const uint32_t u01 = __shfl_sync(0xffffffffu, r1, src0);  // token 2tig + 8
+        const uint32_t u11 = __shfl_sync(0xffffffffu, r1, src1);  // token 2tig + 9
+        bw[nt][0] = __byte_perm(u00, u10, psel);
+        bw[nt][1] = __byte_perm(u01, u11, psel);
+      }
+    };
+    if constexpr (ONEG) weights(0);
+#pragma unroll
+    for (int c2 = 0; c2 < VCH / 2; ++c2) {
+      uint32_t y[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
+      tc::ldsm_x4_trans(vc + vls[c2], y);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * c2 + cc;
+        if constexpr (!ONEG) {
+          if ((VDC * c) % GS == 0) weights((VDC * c) / GS);
+        }
+        // V^T codes of chunk c -> fp16 fragments -> MMAs, in one PTX block
+        if constexpr (V8) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) tc::pv8(y[2 * cc], y[2 * cc + 1], bw[nt], oacc[c][nt]);
+        } else {
+          if constexpr (NT == 1)
+            tc::pv4<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], oacc[2 * c][0], oacc[2 * c + 1][0]);
+          else
+            tc::pv4x2<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], bw[1], oacc[2 * c][0], oacc[2 * c + 1][0],
+                            oacc[2 * c][1], oacc[2 * c + 1][1]);
+        }
+      }
+    }
+  };
+  auto tok0 = [&](int k) { return (cb0 + w + k * NW) * P; };   // absolute token of row 0 of page k
+  auto is_edge = [&](int tb) { return tb < lo || tb + P > L; };
+  // The whole page k in slot sl.
+  auto one_page = [&](int k, int sl) {
+    const int tb = tok0(k);
+    const bool edge = is_edge(tb);
+    float sc[NT][2], p[NT][2], bm[NT];
+    page_scores(sl, tb, edge, sc);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) bm[nt] = fmaxf(sc[nt][0], sc[nt][1]);
+    raise_max(bm);
+    probs(sc, p);
+    page_pv(sl, tb, edge, p);
+  };
+
   int s = 0;   // slot of page k: k % D
+  int k = 0;
+  if constexpr (CL) {
+    // Two pages a step: their Q.K chains are independent, one softmax update
+    // covers 32 tokens, and the wait and the loop control come once per pair.
+    // Pages k, k+1 landed: at most D - 2 younger commit groups pending.
 #pragma unroll 1
-  for (int k = 0; k < n_local; ++k) {
-    const int i = w + k * NW;   // block of the chunk
+    for (; k + 1 < n_local; k += 2) {
+      const int s1 = s + 1 == D ? 0 : s + 1;
+      asm volatile("cp.async.wait_group %0;" ::"n"(D - 2) : "memory");
+      __syncwarp();
+      if (k == k_app || k + 1 == k_app) {
+        place_app(k == k_app ? s : s1);
+        __syncwarp();
+      }
+      if (((valid >> s) & (valid >> s1) & 1u) != 0) {
+        const int ta = tok0(k), tb1 = tok0(k + 1);
+        const bool ea = is_edge(ta), eb = is_edge(tb1);
+        float sa[NT][2], sb[NT][2], pa[NT][2], pb[NT][2], bm[NT];
+        page_scores(s, ta, ea, sa);
+        page_scores(s1, tb1, eb, sb);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) bm[nt] = fmaxf(fmaxf(sa[nt][0], sa[nt][1]), fmaxf(sb[nt][0], sb[nt][1]));
+        raise_max(bm);
+        probs(sa, pa);
+        probs(sb, pb);
+        page_pv(s, ta, ea, pa);
+        page_pv(s1, tb1, eb, pb);
+      } else {   // a page with a bad id: the other one alone
+        if ((valid >> s) & 1u) one_page(k, s);
+        if ((valid >> s1) & 1u) one_page(k + 1, s1);
+      }
+      // both slots are free once every lane is done reading them
+      __syncwarp();
+      if (k + D < n_local) issue(k + D, s);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (k + 1 + D < n_local) issue(k + 1 + D, s1);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      s = s1 + 1 == D ? 0 : s1 + 1;
+    }
+  }
+#pragma unroll 1
+  for (; k < n_local; ++k) {
     // page k landed: at most D - 1 younger commit groups of this lane pending,
     // and the warp's lanes see each other's copies after the sync
     asm volatile("cp.async.wait_group %0;" ::"n"(D - 1) : "memory");
@@ -623,227 +902,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       place_app(s);
       __syncwarp();
     }
-    if ((valid >> s) & 1u) {
-      const uint32_t kc = wring + s * SLOT;
-      const uint32_t vc = kc + KC;
-      const uint32_t kp = kc + KC + VC;
-      const uint32_t vp = kp + KPMAX;
-      const int tb = (cb0 + i) * P;   // absolute token index of the page's row 0
-      const bool edge = tb < lo || tb + P > L;
-
-      // ---- Q.K: A = codes of tokens (gid, gid+8), B = q fragments
-      float s[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = 0.f;
-      float sacc[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-      // fold the accumulated dots of K group g into the scores
-      auto fold = [&](int g) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint32_t pr = kp + (gid + 8 * j) * kprb + g * kstep;
-          const float ks = ld_param<PT>(pr) * (1.0f / kQScale);
-          float kb = 0.f;
-          if constexpr (KAFF) kb = ld_param<PT>(pr + PB);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            float v = ks * fmaf(sacc[nt][2 * j + 1], 1.0f / tc::kLoScale, sacc[nt][2 * j]);
-            if constexpr (KAFF) {
-              float qs = qsum[nt][0];
-#pragma unroll
-              for (int gg = 1; gg < KNG; ++gg)
-                if (gg == g) qs = qsum[nt][gg];
-              v = fmaf(kb, qs, v);
-            }
-            s[nt][j] += v;
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-      };
-#pragma unroll
-      for (int c2 = 0; c2 < KCH / 2; ++c2) {
-        uint32_t r[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
-        tc::ldsm_x4(kc + kls[c2], r);
-        // query fragments of chunks 2c2, 2c2+1: uint4s (K8: one for both, 4-bit: one each)
-        uint32_t qf[NT][2][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int cc = 0; cc < (K8 ? 1 : 2); ++cc) {
-            const int i = K8 ? c2 : 2 * c2 + cc;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(qf[nt][cc][0]), "=r"(qf[nt][cc][1]), "=r"(qf[nt][cc][2]), "=r"(qf[nt][cc][3])
-                         : "r"(qfs + ((nt * (KSTEPS / 2) + i) * 32 + lane) * 16));
-          }
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * c2 + cc;
-          // codes of tokens gid / gid+8 -> fp16 fragments -> MMAs, in one PTX block
-          if constexpr (K8) {   // k-step c: words 2cc, 2cc+1 of the uint4
-            const uint32_t b0[2] = {qf[0][0][2 * cc], qf[0][0][2 * cc + 1]};
-            if constexpr (NT == 1) {
-              tc::qk8(r[2 * cc], r[2 * cc + 1], b0, sacc[0]);
-            } else {
-              const uint32_t b1[2] = {qf[1][0][2 * cc], qf[1][0][2 * cc + 1]};
-              tc::qk8x2(r[2 * cc], r[2 * cc + 1], b0, b1, sacc[0], sacc[1]);
-            }
-          } else {              // k-steps 2c, 2c+1: the uint4 of chunk c
-            const uint32_t be0[2] = {qf[0][cc][0], qf[0][cc][1]}, bo0[2] = {qf[0][cc][2], qf[0][cc][3]};
-            if constexpr (NT == 1) {
-              tc::qk4<KAFF>(r[2 * cc], r[2 * cc + 1], be0, bo0, sacc[0]);
-            } else {
-              const uint32_t be1[2] = {qf[1][cc][0], qf[1][cc][1]}, bo1[2] = {qf[1][cc][2], qf[1][cc][3]};
-              tc::qk4x2<KAFF>(r[2 * cc], r[2 * cc + 1], be0, bo0, be1, bo1, sacc[0], sacc[1]);
-            }
-          }
-          if constexpr (!ONEG) {
-            if ((KDC * (c + 1)) % GS == 0) fold((KDC * c) / GS);
-          }
-        }
-      }
-      if constexpr (ONEG) fold(0);
-      if (edge) {   // the page at the window start or the context end
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int t = tb + gid + 8 * j;
-          if (t < lo || t >= L)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) s[nt][j] = -INFINITY;
-        }
-      }
-
-      // ---- online softmax (base 2), running max raised lazily
-      bool raise = false;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) raise |= fmaxf(s[nt][0], s[nt][1]) > m[nt] + kLazyMax;
-      if (__any_sync(0xffffffffu, raise)) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float bm = fmaxf(s[nt][0], s[nt][1]);
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-          if (bm > m[nt] + kLazyMax) {
-            const float corr = m[nt] == -INFINITY ? 0.f : tc::ex2(m[nt] - bm);
-            l[nt] *= corr;
-#pragma unroll
-            for (int g = 0; g < VNG; ++g) pbias[nt][g] *= corr;
-#pragma unroll
-            for (int t = 0; t < MT; ++t)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) oacc[t][nt][e] *= corr;
-            m[nt] = bm;
-          }
-        }
-      }
-      float p[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float mu = m[nt] == -INFINITY ? 0.f : m[nt];
-        p[nt][0] = tc::ex2(s[nt][0] - mu);   // 0 for masked tokens (s = -inf)
-        p[nt][1] = tc::ex2(s[nt][1] - mu);
-        l[nt] += p[nt][0] + p[nt][1];
-      }
-
-      // ---- P.V: A = V^T codes (ldmatrix.trans), B = weights of V group g.
-      // Entering group g: its scales for the lane's tokens (gid, gid+8), a
-      // raise of its reference when a scale passes half of it (2x headroom),
-      // then w = p * scale * vinv formed here and moved to the B layout.
-      uint32_t bw[NT][2];
-      auto weights = [&](int g) {
-        float vs[2], vb[2] = {0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint32_t pr = vp + (gid + 8 * j) * vprb + g * vstep;
-          vs[j] = ld_param<PT>(pr);
-          if constexpr (VAFF) vb[j] = ld_param<PT>(pr + PB);
-          if (edge) {
-            const int t = tb + gid + 8 * j;
-            if (t < lo || t >= L) vs[j] = vb[j] = 0.f;
-          }
-        }
-        float vig = vinv[0];
-#pragma unroll
-        for (int gg = 1; gg < VNG; ++gg)
-          if (gg == g) vig = vinv[gg];
-        // a scale above half the reference: 2 * scale * vinv > kWScale
-        if (__any_sync(0xffffffffu, 2.0f * fmaxf(vs[0], vs[1]) * vig > kWScale || vig == 0.f)) {
-          float sm = fmaxf(vs[0], vs[1]);
-          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 4));
-          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 8));
-          sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 16));
-          if (sm > 0.f && (vig == 0.f || 2.0f * sm * vig > kWScale)) {
-            const float nvi = kWScale / (2.0f * sm);
-            if (vig > 0.f) {
-              const float ratio = nvi / vig;
-#pragma unroll
-              for (int t = 0; t < MT; ++t) {
-                const int c = V8 ? t : (t >> 1);
-                if ((VDC * c) / GS == g)
-#pragma unroll
-                  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) oacc[t][nt][e] *= ratio;
-              }
-            }
-            vig = nvi;
-#pragma unroll
-            for (int gg = 0; gg < VNG; ++gg)
-              if (gg == g) vinv[gg] = nvi;
-          }
-        }
-        if constexpr (VAFF) {
-#pragma unroll
-          for (int gg = 0; gg < VNG; ++gg)
-            if (gg == g)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                pbias[nt][gg] = fmaf(p[nt][0], vb[0], fmaf(p[nt][1], vb[1], pbias[nt][gg]));
-        }
-        const float w0 = vs[0] * vig, w1 = vs[1] * vig;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint32_t r0 = hilo_pack(p[nt][0] * w0);   // token gid
-          const uint32_t r1 = hilo_pack(p[nt][1] * w1);   // token gid + 8
-          const uint32_t u00 = __shfl_sync(0xffffffffu, r0, src0);  // token 2tig
-          const uint32_t u10 = __shfl_sync(0xffffffffu, r0, src1);  // token 2tig + 1
-          const uint32_t u01 = __shfl_sync(0xffffffffu, r1, src0);  // token 2tig + 8
-          const uint32_t u11 = __shfl_sync(0xffffffffu, r1, src1);  // token 2tig + 9
-          bw[nt][0] = __byte_perm(u00, u10, psel);
-          bw[nt][1] = __byte_perm(u01, u11, psel);
-        }
-      };
-      if constexpr (ONEG) weights(0);
-#pragma unroll
-      for (int c2 = 0; c2 < VCH / 2; ++c2) {
-        uint32_t y[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
-        tc::ldsm_x4_trans(vc + vls[c2], y);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * c2 + cc;
-          if constexpr (!ONEG) {
-            if ((VDC * c) % GS == 0) weights((VDC * c) / GS);
-          }
-          // V^T codes of chunk c -> fp16 fragments -> MMAs, in one PTX block
-          if constexpr (V8) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) tc::pv8(y[2 * cc], y[2 * cc + 1], bw[nt], oacc[c][nt]);
-          } else {
-            if constexpr (NT == 1)
-              tc::pv4<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], oacc[2 * c][0], oacc[2 * c + 1][0]);
-            else
-              tc::pv4x2<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], bw[1], oacc[2 * c][0], oacc[2 * c + 1][0],
-                              oacc[2 * c][1], oacc[2 * c + 1][1]);
-          }
-        }
-      }
-    }
+    if ((valid >> s) & 1u) one_page(k, s);
     // the slot is free once every lane is done reading it: refill it with page k + D
     __syncwarp();
     if (k + D < n_local) issue(k + D, s);
