@@ -339,8 +339,17 @@ def build_layers(args, dev, seed: int) -> list:
                                if cfg.rope != kvq.ROPE_NONE else None)
         for i in range(n):
             layers.append(BenchLayer(w, window, len(layers), dev, gen, args.chunk_tokens, rope_tabs[name]))
+    # One decode step has one seq_lens and one positions array for all layers
+    # of a model, as the model's layers share them; q and the new K/V rows
+    # stay per layer.
+    first = {}
     for L in layers:
         L.use_fused = not args.separate
+        key = (L.w["name"], tuple(L.lens.tolist()))
+        if key in first:
+            L.seq_lens, L.pos = first[key].seq_lens, first[key].pos
+        else:
+            first[key] = L
     return layers
 
 
