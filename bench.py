@@ -70,8 +70,8 @@ def algorithmic_bytes(w: dict, lens: np.ndarray, window: int) -> tuple[int, int]
     return dec, app
 
 
-KERNEL_SOURCES = ("int8_quantized_paged_gb300/csrc/kvq_decode_tc.cuh", "int8_quantized_paged_gb300/csrc/kvq_tc_ptx.cuh",
-                  "int8_quantized_paged_gb300/csrc/kvq_decode.cu", "int8_quantized_paged_gb300/csrc/kvq_quant.cuh")
+KERNEL_SOURCES = tuple("int8_quantized_paged_gb300/csrc/" + f for f in (
+    "kvq_decode_tc.cuh", "kvq_tc_ptx.cuh", "kvq_decode.cu", "kvq_quant.cuh", "kvq_decode_impl.cuh", "kvq_device.cuh"))
 
 
 def kernel_source_hash() -> str:
