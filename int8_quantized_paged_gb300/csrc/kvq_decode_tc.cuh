@@ -198,10 +198,19 @@ __device__ __forceinline__ float hilo_part(float x, int part) {
   const float hi = __half2float(__float2half_rn(x));
   return part ? (x - hi) * tc::kLoScale : x;
 }
+// The same with the low part x - hi not scaled up (it is added to the high
+// part's products in one accumulator).
+__device__ __forceinline__ float hilo_part_unscaled(float x, int part) {
+  const float hi = __half2float(__float2half_rn(x));
+  return part ? x - hi : x;
+}
 
-// KK / VK: code kinds of K and V.  HD: head dim.  NT: 8-column tiles (1 for
-// G <= 4, 2 for G = 8).  NG: scale groups per head (the same for K and V),
-// so every group index below is a compile-time constant.
+// KK / VK: code kinds of K and V.  HD: head dim.  NT: 1 for G <= 4 (one
+// 8-column tile: column 2h the high and 2h+1 the low part of head h), 2 for
+// 4 < G <= 8 (one 8-column tile of the 8 heads, column h head h, run twice:
+// the high parts, then the low parts into the same accumulators).  NG: scale
+// groups per head (the same for K and V), so every group index below is a
+// compile-time constant.
 // PT: stored type of the scales (and biases) of K and V.
 // CL: the cluster mode (kClusterWarps warps per CTA, the chunks of a
 // (sequence, kv head) one cluster of A.cluster CTAs); else kWarps warps.
@@ -234,6 +243,12 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   // 16-byte copies per lane and page: lanes 0-15 copy the K sub-block, 16-31 the V one
   constexpr int NCP = cmax((KC + KPMAX) / 16, (VC + VPMAX) / 16) / 16 + 1;
   static_assert(KCH % 2 == 0 && VCH % 2 == 0, "chunk pairs");
+  // MRG (G > 4): the 8 heads share one tile, the high and low parts are two
+  // passes (the B fragments of pass 0 and 1 take the place of tiles 0 and 1).
+  // A lane's two head slots h2 = 0, 1 are then heads 2 tig + h2 instead of
+  // tig (and 4 + tig), and the P.V accumulators are one tile (NO = 1).
+  constexpr bool MRG = NT == 2;
+  constexpr int NO = MRG ? 1 : NT;
 
   const DecodeArgs& a = A.d;
   const int G = A.G;
@@ -257,12 +272,18 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   const int apos = a.app_pos ? a.app_pos[b] : -1;   // fused append: position of the new row
   float qv[NT][KCH][RUN];
   if (warp == 0) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int hq = NT == 1 ? (gid >> 1) % G : 4 * nt + (gid >> 1);
+    // column gid of the B fragments: head (gid / 2) mod G (NT = 1) or head
+    // gid (MRG: both passes, zero for a column past the last head)
+    const int hq = MRG ? gid : (gid >> 1) % G;
+    if (!MRG || hq < G) {
 #pragma unroll
       for (int c = 0; c < KCH; ++c)
-        load_run<RUN>(a.q, a.act, obase + (int64_t)hq * HD + KDC * c + RUN * tig, qv[nt][c]);
+        load_run<RUN>(a.q, a.act, obase + (int64_t)hq * HD + KDC * c + RUN * tig, qv[0][c]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < KCH; ++c)
+#pragma unroll
+        for (int k = 0; k < RUN; ++k) qv[0][c][k] = 0.f;
     }
   }
   const int CB = A.blocks_per_chunk;
@@ -465,57 +486,60 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     // the RoPE row: the oldest of this lane's D + 1 commit groups
     asm volatile("cp.async.wait_group %0;" ::"n"(D) : "memory");
     __syncwarp();
-    const int part = gid & 1;
     const float sc = a.score_scale * kQScale;
     const int rope = a.rope;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      if (rope == KVQ_ROPE_NORMAL) {   // pairs (2i, 2i+1) lie inside a run
-#pragma unroll
-        for (int c = 0; c < KCH; ++c)
-#pragma unroll
-          for (int k = 0; k < RUN; k += 2) {
-            float2 t;
-            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
-                         : "=f"(t.x), "=f"(t.y) : "r"(rope_s + 4 * (KDC * c + RUN * tig + k)) : "memory");
-            const float x0 = qv[nt][c][k], x1 = qv[nt][c][k + 1];
-            qv[nt][c][k] = x0 * t.x - x1 * t.y;
-            qv[nt][c][k + 1] = x0 * t.y + x1 * t.x;
-          }
-      } else if (rope == KVQ_ROPE_NEOX) {   // pairs (i, i + HD/2): chunk c with chunk c + KCH/2
-#pragma unroll
-        for (int c = 0; c < KCH / 2; ++c)
-#pragma unroll
-          for (int k = 0; k < RUN; ++k) {
-            float2 t;
-            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
-                         : "=f"(t.x), "=f"(t.y) : "r"(rope_s + 8 * (KDC * c + RUN * tig + k)) : "memory");
-            const float x0 = qv[nt][c][k], x1 = qv[nt][c + KCH / 2][k];
-            qv[nt][c][k] = x0 * t.x - x1 * t.y;
-            qv[nt][c + KCH / 2][k] = x0 * t.y + x1 * t.x;
-          }
-      }
+    if (rope == KVQ_ROPE_NORMAL) {   // pairs (2i, 2i+1) lie inside a run
 #pragma unroll
       for (int c = 0; c < KCH; ++c)
 #pragma unroll
-        for (int k = 0; k < RUN; ++k) qv[nt][c][k] *= sc;
-      // B fragments: 4-bit K chunk c, parity p (p = 1 meets 16 * code, so q / 16):
-      //   b0 = q at dims KDC*c + 8tig + p + {0, 4},  b1 = dims + {2, 6}
-      // 8-bit K chunk c:  b0 = dims 16c + 4tig + {0, 2},  b1 = dims + {1, 3}
+        for (int k = 0; k < RUN; k += 2) {
+          float2 t;
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                       : "=f"(t.x), "=f"(t.y) : "r"(rope_s + 4 * (KDC * c + RUN * tig + k)) : "memory");
+          const float x0 = qv[0][c][k], x1 = qv[0][c][k + 1];
+          qv[0][c][k] = x0 * t.x - x1 * t.y;
+          qv[0][c][k + 1] = x0 * t.y + x1 * t.x;
+        }
+    } else if (rope == KVQ_ROPE_NEOX) {   // pairs (i, i + HD/2): chunk c with chunk c + KCH/2
+#pragma unroll
+      for (int c = 0; c < KCH / 2; ++c)
+#pragma unroll
+        for (int k = 0; k < RUN; ++k) {
+          float2 t;
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                       : "=f"(t.x), "=f"(t.y) : "r"(rope_s + 8 * (KDC * c + RUN * tig + k)) : "memory");
+          const float x0 = qv[0][c][k], x1 = qv[0][c + KCH / 2][k];
+          qv[0][c][k] = x0 * t.x - x1 * t.y;
+          qv[0][c + KCH / 2][k] = x0 * t.y + x1 * t.x;
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < KCH; ++c)
+#pragma unroll
+      for (int k = 0; k < RUN; ++k) qv[0][c][k] *= sc;
+    // B fragments of tile (NT = 1) or pass (MRG) nt: 4-bit K chunk c, parity p
+    // (p = 1 meets 16 * code, so q / 16):
+    //   b0 = q at dims KDC*c + 8tig + p + {0, 4},  b1 = dims + {2, 6}
+    // 8-bit K chunk c:  b0 = dims 16c + 4tig + {0, 2},  b1 = dims + {1, 3}
+    // The part: high or low by the column's parity (NT = 1) or by the pass
+    // (MRG, where the low part is not scaled up: both passes add into one
+    // accumulator).
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int part = MRG ? nt : (gid & 1);
+      auto qp = [&](float x) { return MRG ? hilo_part_unscaled(x, part) : hilo_part(x, part); };
       uint32_t qb[KSTEPS][2];
 #pragma unroll
       for (int c = 0; c < KCH; ++c) {
         if constexpr (K8) {
-          qb[c][0] = tc::pack_half2(hilo_part(qv[nt][c][0], part), hilo_part(qv[nt][c][2], part));
-          qb[c][1] = tc::pack_half2(hilo_part(qv[nt][c][1], part), hilo_part(qv[nt][c][3], part));
+          qb[c][0] = tc::pack_half2(qp(qv[0][c][0]), qp(qv[0][c][2]));
+          qb[c][1] = tc::pack_half2(qp(qv[0][c][1]), qp(qv[0][c][3]));
         } else {
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             const float f = p ? 1.0f / 16.0f : 1.0f;
-            qb[2 * c + p][0] =
-                tc::pack_half2(hilo_part(qv[nt][c][p] * f, part), hilo_part(qv[nt][c][p + 4] * f, part));
-            qb[2 * c + p][1] =
-                tc::pack_half2(hilo_part(qv[nt][c][p + 2] * f, part), hilo_part(qv[nt][c][p + 6] * f, part));
+            qb[2 * c + p][0] = tc::pack_half2(qp(qv[0][c][p] * f), qp(qv[0][c][p + 4] * f));
+            qb[2 * c + p][1] = tc::pack_half2(qp(qv[0][c][p + 2] * f), qp(qv[0][c][p + 6] * f));
           }
         }
       }
@@ -524,30 +548,30 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qfs + ((nt * (KSTEPS / 2) + i) * 32 + lane) * 16),
                      "r"(qb[2 * i][0]), "r"(qb[2 * i][1]), "r"(qb[2 * i + 1][0]), "r"(qb[2 * i + 1][1])
                      : "memory");
-      // affine K: per-group q sums of the tile's heads, [nt][g][4] (lane 8h holds
-      // head h of the tile: gid = 2h, part hi)
-      if constexpr (KAFF) {
-        float part_sum[KNG];
+    }
+    // affine K: per-group q sums of the columns' heads: [g][4] at lane 8h for
+    // head h (gid = 2h, NT = 1), [g][8] at lane 4h for head h (MRG)
+    if constexpr (KAFF) {
+      float part_sum[KNG];
 #pragma unroll
-        for (int g = 0; g < KNG; ++g) part_sum[g] = 0.f;
+      for (int g = 0; g < KNG; ++g) part_sum[g] = 0.f;
 #pragma unroll
-        for (int c = 0; c < KCH; ++c) {
-          const int g = (KDC * c) / GS;
+      for (int c = 0; c < KCH; ++c) {
+        const int g = (KDC * c) / GS;
 #pragma unroll
-          for (int gg = 0; gg < KNG; ++gg)
-            if (gg == g)
+        for (int gg = 0; gg < KNG; ++gg)
+          if (gg == g)
 #pragma unroll
-              for (int k = 0; k < RUN; ++k) part_sum[gg] += qv[nt][c][k];
-        }
+            for (int k = 0; k < RUN; ++k) part_sum[gg] += qv[0][c][k];
+      }
 #pragma unroll
-        for (int g = 0; g < KNG; ++g) {
-          float v = part_sum[g];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          if (tig == 0 && (gid & 1) == 0)
-            asm volatile("st.shared.f32 [%0], %1;" ::"r"(qsum_s + 4 * ((nt * KNG + g) * 4 + (gid >> 1))),
-                         "f"(v * (1.0f / kQScale))
-                         : "memory");
+      for (int g = 0; g < KNG; ++g) {
+        float v = part_sum[g];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (tig == 0 && (MRG || (gid & 1) == 0)) {
+          const int slot = MRG ? g * 8 + gid : g * 4 + (gid >> 1);
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(qsum_s + 4 * slot), "f"(v * (1.0f / kQScale)) : "memory");
         }
       }
     }
@@ -560,7 +584,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     __syncwarp();
   }
   __syncthreads();
-  // affine K: the q sums of this lane's score head 4nt + tig (mod G)
+  // affine K: the q sums of this lane's score heads: tig (mod G) for NT = 1,
+  // 2 tig + h2 for head slot h2 (MRG)
   float qsum[NT][KNG];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -568,9 +593,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     for (int g = 0; g < KNG; ++g) {
       qsum[nt][g] = 0.f;
       if constexpr (KAFF) {
-        const int hs = NT == 1 ? tig % G : tig;
-        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qsum[nt][g]) : "r"(qsum_s + 4 * ((nt * KNG + g) * 4 + hs))
-                     : "memory");
+        const int slot = MRG ? g * 8 + 2 * tig + nt : g * 4 + tig % G;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qsum[nt][g]) : "r"(qsum_s + 4 * slot) : "memory");
       }
     }
 
@@ -586,15 +610,18 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   for (int c = 0; c < KCH; c += 2) kls[c / 2] = swz<KRB>(trow, c + (mi >> 1));
 #pragma unroll
   for (int c = 0; c < VCH; c += 2) vls[c / 2] = swz<VRB>(trow, c + (mi >> 1));
-  // P.V transposition: the B column of this lane is head hq (part gid % 2);
-  // its tokens 2tig, 2tig+1 (+8) come from lanes src0, src1.
-  const int src_tig = NT == 1 ? (gid >> 1) % G : (gid >> 1);
+  // P.V transposition: the B column of this lane is head (gid / 2) mod G,
+  // part gid % 2 (NT = 1), or head gid (MRG); its tokens 2tig, 2tig+1 (+8)
+  // come from lanes src0, src1, which hold them for heads 2 src_tig, +1 (MRG)
+  // or the head's two parts (NT = 1) in the two halves of one word.
+  const int src_tig = MRG ? (gid >> 1) : (gid >> 1) % G;
   const int src0 = 8 * tig + src_tig, src1 = src0 + 4;
   const uint32_t psel = (gid & 1) ? 0x7632u : 0x5410u;
 
-  // ---- running state: head 4nt + tig (mod G) of this lane
+  // ---- running state of head slot h2 of this lane: head tig (mod G) for
+  // NT = 1, head 2 tig + h2 for MRG
   float m[NT], l[NT];
-  float oacc[MT][NT][4];
+  float oacc[MT][NO][4];   // MRG: elements e of head slot e & 1
   float pbias[NT][VNG];   // affine V: sum of p * bias per group
   float vinv[VNG];        // 2^7 / R, R the reference V scale of the group (0: none yet)
 #pragma unroll
@@ -603,11 +630,26 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     l[nt] = 0.f;
 #pragma unroll
     for (int g = 0; g < VNG; ++g) pbias[nt][g] = 0.f;
+  }
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int o = 0; o < NO; ++o)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oacc[t][o][e] = 0.f;
+  // the P.V accumulators of head slot h2 scaled by f
+  auto scale_slot = [&](int h2, float f) {
 #pragma unroll
     for (int t = 0; t < MT; ++t)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) oacc[t][nt][e] = 0.f;
-  }
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (MRG) {
+          if ((e & 1) == h2) oacc[t][0][e] *= f;
+        } else {
+          oacc[t][h2][e] *= f;
+        }
+      }
+  };
 #pragma unroll
   for (int g = 0; g < VNG; ++g) vinv[g] = 0.f;
 
@@ -634,7 +676,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         if constexpr (KAFF) kb = ld_param<PT>(pr + PB);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          float v = ks * fmaf(sacc[nt][2 * j + 1], 1.0f / tc::kLoScale, sacc[nt][2 * j]);
+          // MRG: pass 0 (high) and pass 1 (low) of head slot nt; NT = 1: the
+          // high and the (scaled) low column of the head
+          float v = MRG ? ks * (sacc[0][2 * j + nt] + sacc[1][2 * j + nt])
+                        : ks * fmaf(sacc[nt][2 * j + 1], 1.0f / tc::kLoScale, sacc[nt][2 * j]);
           if constexpr (KAFF) {
             float qs = qsum[nt][0];
 #pragma unroll
@@ -720,10 +765,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
           l[nt] *= corr;
 #pragma unroll
           for (int g = 0; g < VNG; ++g) pbias[nt][g] *= corr;
-#pragma unroll
-          for (int t = 0; t < MT; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) oacc[t][nt][e] *= corr;
+          scale_slot(nt, corr);
           m[nt] = x;
         }
       }
@@ -779,9 +821,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
               const int c = V8 ? t : (t >> 1);
               if ((VDC * c) / GS == g)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int o = 0; o < NO; ++o)
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) oacc[t][nt][e] *= ratio;
+                  for (int e = 0; e < 4; ++e) oacc[t][o][e] *= ratio;
             }
           }
           vig = nvi;
@@ -799,10 +841,28 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
               pbias[nt][gg] = fmaf(p[nt][0], vb[0], fmaf(p[nt][1], vb[1], pbias[nt][gg]));
       }
       const float w0 = vs[0] * vig, w1 = vs[1] * vig;
+      // MRG: words of pass nt hold the part nt of heads 2tig, 2tig+1 (the
+      // low part not scaled up); NT = 1: both parts of head tig
+      uint32_t rp[NT][2];
+      if constexpr (MRG) {
+        const float x00 = p[0][0] * w0, x10 = p[1][0] * w0;   // token gid, heads 2tig, 2tig+1
+        const float x01 = p[0][1] * w1, x11 = p[1][1] * w1;   // token gid + 8
+        const float h00 = __half2float(__float2half_rn(x00)), h10 = __half2float(__float2half_rn(x10));
+        const float h01 = __half2float(__float2half_rn(x01)), h11 = __half2float(__float2half_rn(x11));
+        rp[0][0] = tc::pack_half2(h00, h10);
+        rp[0][1] = tc::pack_half2(h01, h11);
+        rp[1][0] = tc::pack_half2(x00 - h00, x10 - h10);
+        rp[1][1] = tc::pack_half2(x01 - h01, x11 - h11);
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          rp[nt][0] = hilo_pack(p[nt][0] * w0);   // token gid
+          rp[nt][1] = hilo_pack(p[nt][1] * w1);   // token gid + 8
+        }
+      }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t r0 = hilo_pack(p[nt][0] * w0);   // token gid
-        const uint32_t r1 = hilo_pack(p[nt][1] * w1);   // token gid + 8
+        const uint32_t r0 = rp[nt][0], r1 = rp[nt][1];
         const uint32_t u00 = __shfl_sync(0xffffffffu, r0, src0);  // token 2tig
         const uint32_t u10 = __shfl_sync(0xffffffffu, r0, src1);  // token 2tig + 1
         const uint32_t u01 = __shfl_sync(0xffffffffu, r1, src0);  // token 2tig + 8
@@ -823,15 +883,14 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
           if ((VDC * c) % GS == 0) weights((VDC * c) / GS);
         }
         // V^T codes of chunk c -> fp16 fragments -> MMAs, in one PTX block
-        if constexpr (V8) {
+        if constexpr (V8) {   // MRG: both passes into tile 0
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) tc::pv8(y[2 * cc], y[2 * cc + 1], bw[nt], oacc[c][nt]);
+          for (int nt = 0; nt < NT; ++nt) tc::pv8(y[2 * cc], y[2 * cc + 1], bw[nt], oacc[c][MRG ? 0 : nt]);
         } else {
           if constexpr (NT == 1)
             tc::pv4<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], oacc[2 * c][0], oacc[2 * c + 1][0]);
           else
-            tc::pv4x2<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], bw[1], oacc[2 * c][0], oacc[2 * c + 1][0],
-                            oacc[2 * c][1], oacc[2 * c + 1][1]);
+            tc::pv4m<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], bw[1], oacc[2 * c][0], oacc[2 * c + 1][0]);
         }
       }
     }
@@ -931,7 +990,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       v += __shfl_xor_sync(0xffffffffu, v, 16);
       pbs[g] = v;
     }
-    const int h = 4 * nt + tig;   // head owned by this lane (valid when < G)
+    const int h = MRG ? 2 * tig + nt : 4 * nt + tig;   // head of slot nt (valid when < G)
     if (h < G) {
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
@@ -956,8 +1015,18 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
             pbg = pbs[gg];
           }
         const float sc = vi > 0.f ? f / vi : 0.f;   // R / 2^7, with 1/16 for 16 * code
-        ows[(w * G + h) * HD + d0] = fmaf(fmaf(oacc[t][nt][1], 1.0f / tc::kLoScale, oacc[t][nt][0]), sc, pbg);
-        ows[(w * G + h) * HD + d1] = fmaf(fmaf(oacc[t][nt][3], 1.0f / tc::kLoScale, oacc[t][nt][2]), sc, pbg);
+        // rows gid / gid+8 of the tile are dims d0 / d1; MRG: columns 2tig, 2tig+1
+        // are heads 2tig, 2tig+1; NT = 1: the high and the low part of head tig
+        float o0, o1;
+        if constexpr (MRG) {
+          o0 = oacc[t][0][nt];
+          o1 = oacc[t][0][2 + nt];
+        } else {
+          o0 = fmaf(oacc[t][nt][1], 1.0f / tc::kLoScale, oacc[t][nt][0]);
+          o1 = fmaf(oacc[t][nt][3], 1.0f / tc::kLoScale, oacc[t][nt][2]);
+        }
+        ows[(w * G + h) * HD + d0] = fmaf(o0, sc, pbg);
+        ows[(w * G + h) * HD + d1] = fmaf(o1, sc, pbg);
       }
       if (gid == 0) {
         mws[w * G + h] = m[nt];

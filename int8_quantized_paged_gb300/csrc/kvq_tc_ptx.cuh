@@ -320,6 +320,22 @@ __device__ __forceinline__ void pv4x2(uint32_t y0, uint32_t y8, const uint32_t (
                  "r"(q4_magic_hi<AFF>()));
 }
 
+// P.V, 4-bit V, one tile run twice (weights b, then c) into the same
+// accumulators: the high and the low parts of the weights.
+template <bool AFF>
+__device__ __forceinline__ void pv4m(uint32_t y0, uint32_t y8, const uint32_t (&b)[2], const uint32_t (&c)[2],
+                                     float (&de)[4], float (&dodd)[4]) {
+  asm volatile("{\n" KVQ_Q4_PRE("%14", "%15", "%8", "%9")
+               KVQ_MMA("%0,%1,%2,%3", "a0", "a2", "a1", "a3", "%10", "%11")
+               KVQ_MMA("%4,%5,%6,%7", "e0", "e2", "e1", "e3", "%10", "%11")
+               KVQ_MMA("%0,%1,%2,%3", "a0", "a2", "a1", "a3", "%12", "%13")
+               KVQ_MMA("%4,%5,%6,%7", "e0", "e2", "e1", "e3", "%12", "%13") "}\n"
+               : "+f"(de[0]), "+f"(de[1]), "+f"(de[2]), "+f"(de[3]), "+f"(dodd[0]), "+f"(dodd[1]),
+                 "+f"(dodd[2]), "+f"(dodd[3])
+               : "r"(y0), "r"(y8), "r"(b[0]), "r"(b[1]), "r"(c[0]), "r"(c[1]), "r"(q4_magic_lo<AFF>()),
+                 "r"(q4_magic_hi<AFF>()));
+}
+
 // 8-bit codes: x = bytes b0..b3 -> (b0, b2) and (b1, b3) as fp16 (XOR 0x80,
 // mantissa of 1024, minus 1152).
 #define KVQ_Q8_PRE(K0, X0, X8)                                               \

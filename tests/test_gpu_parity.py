@@ -190,3 +190,24 @@ def test_group16_runs_on_cuda_core_kernel():
     ref = c.oracle_decode(q)
     for chunk in (0, 64):
         assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), ref) <= TOL
+
+
+@pytest.mark.parametrize("chunk", [0, 64])
+@pytest.mark.parametrize("heads", [(64, 8), (32, 4)])
+def test_wide_query_groups_match_oracle(heads, chunk):
+    """G = 8 query heads per kv head with 4-bit K and V: the 8 heads share one
+    MMA tile, the high and low parts of q and of the weights as two passes."""
+    w = wl.workload("llama8b", batch=2, n_heads=heads[0], n_kv_heads=heads[1])
+    c = Case(w, [700, 33])
+    q = c.queries()
+    assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q)) <= TOL
+    assert c.cache.status_bits() == 0
+
+
+def test_wide_query_group_affine_matches_oracle():
+    """G = 8 with affine 4-bit K/V (per-group q sums of the 8 heads)."""
+    w = wl.workload("gemma_mix", batch=2, n_heads=64, n_kv_heads=8, head_dim=128)
+    c = Case(w, [900, 17])
+    q = c.queries()
+    for chunk in (0, 64):
+        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q)) <= TOL
