@@ -42,7 +42,8 @@
 //         w is formed where p lives and moved into the B layout with four
 //         shuffles.
 // Each warp keeps its own (m, l, O); the warps merge through shared memory at
-// the end.  G = 8 uses two 8-column tiles (NT = 2).
+// the end.  G = 8 (NT = 2) puts the 8 heads in the 8 columns of one tile and
+// runs the high and the low parts as two passes into the same accumulators.
 #pragma once
 
 #include <cuda.h>
