@@ -364,80 +364,89 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
 
-  // ---- fused append.  The warp that reads the page of absolute block
-  // apos / P (in the chunk that holds it; for a ring, the ring page that block
-  // lives in, whose other rows a window no longer than the ring reads only
-  // through the same block) stages the new K and V rows and the RoPE row of
-  // their position in shared memory now, as its own commit group ahead of
-  // its pages.  When it reaches that page it quantizes the rows (tc_append_row,
-  // the append kernel's arithmetic) and writes them into the pool and over
-  // the row's stale copy in the page's slot, so no read of the pool has to
-  // wait for the write.  A position outside the attended blocks is written by
-  // warp 0 of chunk 0 in the prologue.
+  // ---- fused append.  The CTA whose chunk holds the page of absolute block
+  // apos / P (for a ring, the ring page that block lives in, whose other rows
+  // a window no longer than the ring reads only through the same block)
+  // writes the new row; for a position outside the attended blocks, chunk 0
+  // does.  Two of its warps that build no query fragments share the work:
+  // warp NW-1 stages the K row and the RoPE row of its position, warp NW-2 the
+  // V row, each as its own commit group ahead of its pages; while the pages
+  // are in flight each quantizes its row (tc_append_row, the append kernel's
+  // arithmetic) into the pool and into a row buffer in shared memory.  The
+  // warp that reads the page copies the buffers over the row's stale copy in
+  // its slot when it gets there (after the barrier that ends the prologue),
+  // so no read of the pool waits for the write.
   const int app_off = NW * D * SLOT + tc_qfrag_bytes(HD, NT) + 4 * HD + 16 * NT * NG;   // [K][V][RoPE]
-  int k_app = -1;    // this warp's page index of the new row; -2: write it in the prologue
+  int k_app = -1;    // the page warp: its page index of the new row
+  int app_role = 0;  // 1: this warp quantizes the K row, 2: the V row
   int app_pg = -1;   // page id of the new row's block
   if (a.app_pos) {
     const bool pos_ok = apos >= 0 && (ring > 0 || apos / P < a.max_pages) &&
                         (a.rope == KVQ_ROPE_NONE || apos < a.rope_max_pos);
     const int bp = apos / P;
+    bool writer = false;   // this CTA writes the row
     if (!pos_ok) {
       if (chunk == 0 && tid == 0) report(a.status, KVQ_DEV_BAD_POS);
     } else if (bp >= blk_lo && bp < blk_hi) {
-      if (chunk == (bp - blk_lo) / CB && w == (bp - cb0) % NW) k_app = (bp - cb0) / NW;
-    } else if (chunk == 0 && w == 0) {
-      k_app = -2;
+      writer = chunk == (bp - blk_lo) / CB;
+      if (writer && w == (bp - cb0) % NW) k_app = (bp - cb0) / NW;
+    } else {
+      writer = chunk == 0;
     }
-    if (k_app != -1) {
+    if (writer) {
       app_pg = bt[ring > 0 ? (int)(((int64_t)bp * P) % ring) / P : bp];   // a ring keeps the block in a ring page
       if (app_pg < 0 || app_pg >= npp) {
-        report(a.status, KVQ_DEV_BAD_PAGE);
+        if (tid == 0) report(a.status, KVQ_DEV_BAD_PAGE);
         k_app = -1;
+      } else {
+        app_role = w == NW - 1 ? 1 : (w == NW - 2 ? 2 : 0);
       }
     }
-    if (k_app != -1) {
+    if (app_role != 0) {
       const int actb = a.act == KVQ_F32 ? 4 : 2;
       const int64_t row = ((int64_t)b * a.n_kv_heads + kvh) * HD * actb;
-      const uint8_t* ks = static_cast<const uint8_t*>(a.app_k) + row;
-      const uint8_t* vs = static_cast<const uint8_t*>(a.app_v) + row;
-      const uint8_t* cs = reinterpret_cast<const uint8_t*>(a.rope_tab) + (int64_t)apos * (4 * HD);
-      const uint32_t dst = tc::smem_u32(smem) + app_off;
-      for (int j = lane; j < HD * actb / 16; j += 32) {
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * j), "l"(ks + 16 * j) : "memory");
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 4 * HD + 16 * j), "l"(vs + 16 * j)
-                     : "memory");
-      }
-      if (a.rope != KVQ_ROPE_NONE)
+      const uint8_t* src = static_cast<const uint8_t*>(app_role == 1 ? a.app_k : a.app_v) + row;
+      const uint32_t dst = tc::smem_u32(smem) + app_off + (app_role == 1 ? 0 : 4 * HD);
+      for (int j = lane; j < HD * actb / 16; j += 32)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * j), "l"(src + 16 * j) : "memory");
+      if (app_role == 1 && a.rope != KVQ_ROPE_NONE) {
+        const uint8_t* cs = reinterpret_cast<const uint8_t*>(a.rope_tab) + (int64_t)apos * (4 * HD);
+        const uint32_t cdst = tc::smem_u32(smem) + app_off + 8 * HD;
         for (int j = lane; j < HD / 4; j += 32)
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 8 * HD + 16 * j), "l"(cs + 16 * j)
-                       : "memory");
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(cdst + 16 * j), "l"(cs + 16 * j) : "memory");
+      }
       asm volatile("cp.async.commit_group;" ::: "memory");
     }
   }
   // The quantized rows, in the pool's row format, after the staged rows:
   // K codes [KRB], V codes [VRB], K parameter row, V parameter row.
   const int qk_off = app_off + 12 * HD, qv_off = qk_off + KRB, qkp_off = qv_off + VRB, qvp_off = qkp_off + 64;
-  // Quantizes the staged rows (their copies have landed) into the pool and
-  // into the row buffers above.
+  // Quantizes this warp's staged row (its copies have landed) into the pool
+  // and into its row buffer above.
   auto quantize_app = [&]() {
     const uint8_t* st = smem + app_off;
-    const float2* cs = a.rope != KVQ_ROPE_NONE ? reinterpret_cast<const float2*>(st + 8 * HD) : nullptr;
     const int r = apos % P;
-    const RowCodes kq = tc_append_row<HD>(st, a.act, cs, a.rope, a.kl, lane);
-    const RowCodes vq = tc_append_row<HD>(st + 4 * HD, a.act, nullptr, a.rope, a.vl, lane);
-    store_row(kq, a.kl, const_cast<uint8_t*>(a.k_pool) + (int64_t)app_pg * a.kl.page_bytes + (int64_t)kvh * a.kl.sub_bytes,
-              r, lane);
-    store_row(vq, a.vl, const_cast<uint8_t*>(a.v_pool) + (int64_t)app_pg * a.vl.page_bytes + (int64_t)kvh * a.vl.sub_bytes,
-              r, lane);
-    store_code_bytes(smem + qk_off + lane * kq.nbytes, kq.w, kq.nbytes);
-    store_code_bytes(smem + qv_off + lane * vq.nbytes, vq.w, vq.nbytes);
-    if (kq.leader) {
-      store_param(smem + qkp_off + param_scale_offset(a.kl, kq.group), a.kl.param, kq.scale);
-      if (KAFF) store_param(smem + qkp_off + param_bias_offset(a.kl, kq.group), a.kl.param, kq.bias);
-    }
-    if (vq.leader) {
-      store_param(smem + qvp_off + param_scale_offset(a.vl, vq.group), a.vl.param, vq.scale);
-      if (VAFF) store_param(smem + qvp_off + param_bias_offset(a.vl, vq.group), a.vl.param, vq.bias);
+    if (app_role == 1) {
+      const float2* cs = a.rope != KVQ_ROPE_NONE ? reinterpret_cast<const float2*>(st + 8 * HD) : nullptr;
+      const RowCodes kq = tc_append_row<HD>(st, a.act, cs, a.rope, a.kl, lane);
+      store_row(kq, a.kl,
+                const_cast<uint8_t*>(a.k_pool) + (int64_t)app_pg * a.kl.page_bytes + (int64_t)kvh * a.kl.sub_bytes,
+                r, lane);
+      store_code_bytes(smem + qk_off + lane * kq.nbytes, kq.w, kq.nbytes);
+      if (kq.leader) {
+        store_param(smem + qkp_off + param_scale_offset(a.kl, kq.group), a.kl.param, kq.scale);
+        if (KAFF) store_param(smem + qkp_off + param_bias_offset(a.kl, kq.group), a.kl.param, kq.bias);
+      }
+    } else {
+      const RowCodes vq = tc_append_row<HD>(st + 4 * HD, a.act, nullptr, a.rope, a.vl, lane);
+      store_row(vq, a.vl,
+                const_cast<uint8_t*>(a.v_pool) + (int64_t)app_pg * a.vl.page_bytes + (int64_t)kvh * a.vl.sub_bytes,
+                r, lane);
+      store_code_bytes(smem + qv_off + lane * vq.nbytes, vq.w, vq.nbytes);
+      if (vq.leader) {
+        store_param(smem + qvp_off + param_scale_offset(a.vl, vq.group), a.vl.param, vq.scale);
+        if (VAFF) store_param(smem + qvp_off + param_bias_offset(a.vl, vq.group), a.vl.param, vq.bias);
+      }
     }
   };
   // Writes the quantized rows over row apos % P of slot s (codes swizzled
@@ -577,9 +586,11 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       }
     }
   }
-  // The new row is quantized now, while the warp's pages are still arriving.
-  if (k_app != -1) {
-    asm volatile("cp.async.wait_group %0;" ::"n"(D) : "memory");   // the staged rows: older than the pages
+  // The new row is quantized now, while the pages are still arriving, by the
+  // two appender warps in parallel with warp 0's fragments; the barrier below
+  // publishes the row buffers to the page warp.
+  if (app_role != 0) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(D) : "memory");   // the staged row: older than the pages
     __syncwarp();
     quantize_app();
     __syncwarp();

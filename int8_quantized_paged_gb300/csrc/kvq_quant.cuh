@@ -45,6 +45,19 @@ __device__ __forceinline__ void rope_rotate_row(float (&x)[DPL], const float2* c
   }
 }
 
+// rint(fl(x / s)) (round half to even of the correctly rounded quotient), for
+// |x / s| <= 2^7 + 1 and s > 0, mostly without a division: y = fl(x * r) with
+// r = fl(1 / s) is within 2^-23 |x / s| + 2^-24 |x / s| of fl(x / s), under
+// 2^-15 for these quotients.  So unless y lies within 2^-14 of a rounding
+// boundary n + 1/2, both round to the same integer; near one the quotient is
+// taken exactly.
+__device__ __forceinline__ float rint_quotient(float x, float s, float r) {
+  const float y = __fmul_rn(x, r);
+  const float t = y - floorf(y);   // exact for |y| < 2^23
+  if (fabsf(t - 0.5f) > 6.103515625e-05f) return rintf(y);
+  return rintf(__fdiv_rn(x, s));
+}
+
 // The lane's quantized row piece: its packed code bytes (DPL/2 for 4-bit
 // kinds, DPL for 8-bit, little-endian in w) and its group's parameters.
 struct RowCodes {
@@ -74,9 +87,10 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
     }
     const float scale = round_param(__fdiv_rn(__fsub_rn(mx, mn), 15.0f), L.param);
     const float bias = round_param(mn, L.param);
+    const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
 #pragma unroll
     for (int j = 0; j < DPL; ++j) {
-      float y = scale == 0.0f ? 0.0f : rintf(__fdiv_rn(__fsub_rn(x[j], bias), scale));
+      float y = scale == 0.0f ? 0.0f : rint_quotient(__fsub_rn(x[j], bias), scale, rs);
       y = fminf(fmaxf(y, 0.0f), 15.0f);
       c[j] = (int)y;
     }
@@ -90,9 +104,10 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
     for (int o = 1; o < lpg; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float floor_s = L.param == KVQ_F16 ? 6.103515625e-05f : 1e-8f;
     const float scale = round_param(fmaxf(__fdiv_rn(amax, qmax), floor_s), L.param);
+    const float rs = __frcp_rn(scale);
 #pragma unroll
     for (int j = 0; j < DPL; ++j) {
-      float y = rintf(__fdiv_rn(x[j], scale));
+      float y = rint_quotient(x[j], scale, rs);
       y = fminf(fmaxf(y, -qmax), qmax);
       c[j] = (int)y;
     }
