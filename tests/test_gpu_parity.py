@@ -9,8 +9,9 @@ import pytest
 import torch
 
 import kvq_workloads as wl
-from gpu_cases import TOL, Case, max_row_err
+from gpu_cases import TOL, Case, max_row_err, oracle_rope
 from int8_quantized_paged_gb300 import kvq
+from int8_quantized_paged_gb300.cache import LayerCache
 from oracle import kvq_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -211,3 +212,65 @@ def test_wide_query_group_affine_matches_oracle():
     q = c.queries()
     for chunk in (0, 64):
         assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q)) <= TOL
+
+
+def _tie_rows(w: dict, n_rows: int, seed: int) -> np.ndarray:
+    """Rows whose quotients x / scale land on, and one or two ulps beside,
+    half-integers: each group's largest magnitude is qmax * s for a random s,
+    so the stored scale is (close to) s, and the other elements are
+    (k + 1/2) * scale for the scale the quantizer will store."""
+    rng = np.random.default_rng(seed)
+    hkv, hd, g = w["n_kv_heads"], w["head_dim"], w["k_group"]
+    qmax = 127.0 if w["k_kind"] == "sym8" else 7.0
+    rows = np.zeros((n_rows, hkv, hd), np.float32)
+    for r in range(n_rows):
+        for h in range(hkv):
+            for g0 in range(0, hd, g):
+                s = np.float32(rng.uniform(0.05, 3.0))
+                amax = np.float32(qmax) * s
+                scale = np.float32(np.float32(amax) / np.float32(qmax))
+                if w["k_param"] == "f16":
+                    scale = np.float32(np.float16(scale))
+                ks = rng.integers(-int(qmax), int(qmax), g).astype(np.float32) + np.float32(0.5)
+                x = (ks * scale).astype(np.float32)
+                nudge = rng.integers(-2, 3, g)
+                x = np.array([np.nextafter(v, np.float32(np.inf) if d > 0 else np.float32(-np.inf))
+                              if d else v for v, d in zip(x, nudge)], np.float32)
+                x[0] = amax * (1 if rng.random() < 0.5 else -1)
+                rows[r, h, g0:g0 + g] = np.clip(x, -amax, amax)
+    return rows
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", dict(rope="none")),
+    ("long_mixed", dict(rope="none", act="f32", k_kind="sym8", v_kind="sym8")),
+])
+def test_append_codes_at_rounding_ties(name, over):
+    """Codes of quotients at and next to rounding ties: the append kernel and
+    the fused call write the oracle's bytes (the division-free quotient falls
+    back to the exact one there)."""
+    w = wl.workload(name, batch=1, **over)
+    cfg = kvq.config(**w)
+    spec = O.Spec.from_workload(w)
+    n = 48
+    cache = LayerCache(cfg, 1, 4, 4, rope_max_pos=n + 1)
+    cache.reserve(0, n)
+    cache.sync_table()
+    bt = cache.table.data()
+    k, v = _tie_rows(w, n, 1), _tie_rows(w, n, 2)
+    dev = cache.device
+    cache.append(torch.from_numpy(k[:n - 1]).to(dev), torch.from_numpy(v[:n - 1]).to(dev),
+                 torch.arange(n - 1, dtype=torch.int32, device=dev),
+                 torch.zeros(n - 1, dtype=torch.int32, device=dev))
+    # the last row through the fused call
+    q = torch.from_numpy(wl.queries(dict(w, batch=1)).astype(np.float32)).to(dev)
+    out = torch.empty_like(q)
+    cache.append_decode(q, torch.from_numpy(k[n - 1:]).to(dev), torch.from_numpy(v[n - 1:]).to(dev),
+                        torch.tensor([n - 1], dtype=torch.int32, device=dev),
+                        torch.tensor([n], dtype=torch.int32, device=dev), out, cache.workspace(1))
+    torch.cuda.synchronize()
+    assert cache.status_bits() == 0
+    pools = {"k": np.zeros(4 * O.page_bytes(spec, "k"), np.uint8), "v": np.zeros(4 * O.page_bytes(spec, "v"), np.uint8)}
+    O.append(spec, pools, k, v, np.zeros(n, np.int64), np.arange(n), bt, 0, oracle_rope(spec.head_dim, spec.rope_base, n + 1))
+    assert np.array_equal(cache.k_pool.cpu().numpy(), pools["k"])
+    assert np.array_equal(cache.v_pool.cpu().numpy(), pools["v"])
