@@ -127,7 +127,7 @@ static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens,
   if (blocks > (int64_t)kMaxCluster * kClusterWarps * max_ppw || (int64_t)batch * c.n_kv_heads > 4 * num_sms())
     return false;
   // the warps' merge, then the CTA's partial o [G][hd] and (m, l) [G]
-  size_t need = (size_t)kClusterWarps * G * (hd + 2) * sizeof(float);
+  size_t need = ((size_t)kClusterWarps * G * (hd + 2) + G) * sizeof(float);
   need = ((need + 15) & ~(size_t)15) + (size_t)G * hd * sizeof(float) + (size_t)G * 2 * sizeof(float);
   size_t smem = (size_t)kClusterWarps * ring + pre;
   if (smem < need) smem = need;
@@ -334,7 +334,7 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     // cluster's partial or the combine's weights.
     const size_t ring = tc_ring_bytes(*cfg);
     const size_t pre = tc_pre_bytes(hd, nt, ng);
-    auto merge_bytes = [&](int warps) { return (size_t)warps * G * (hd + 2) * sizeof(float); };
+    auto merge_bytes = [&](int warps) { return ((size_t)warps * G * (hd + 2) + G) * sizeof(float); };
     TcLaunchCfg lc{};
     lc.stream = stream;
     lc.pdl = pdl_enabled();

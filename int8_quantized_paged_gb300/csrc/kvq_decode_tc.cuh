@@ -982,11 +982,20 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   }
 
   // ---- merge the warps' states (shared memory reused once every warp is
-  // past its ring; no copies are pending)
+  // past its ring; no copies are pending).  First the warps' running maxima,
+  // then each warp's partial (o, l) scaled by 2^(m_w - M) with M the CTA's
+  // maximum (0 for a warp that saw no key), so the merge itself is a sum.
   __syncthreads();
   float* ows = reinterpret_cast<float*>(smem);   // [NW][G][HD]
   float* mws = ows + NW * G * HD;                // [NW][G]
   float* lws = mws + NW * G;                     // [NW][G]
+  float* Mh = lws + NW * G;                      // [G]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = MRG ? 2 * tig + nt : 4 * nt + tig;   // head of slot nt (valid when < G)
+    if (h < G && gid == 0) mws[w * G + h] = m[nt];
+  }
+  __syncthreads();
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     float lt = l[nt];
@@ -1002,8 +1011,12 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       v += __shfl_xor_sync(0xffffffffu, v, 16);
       pbs[g] = v;
     }
-    const int h = MRG ? 2 * tig + nt : 4 * nt + tig;   // head of slot nt (valid when < G)
+    const int h = MRG ? 2 * tig + nt : 4 * nt + tig;
     if (h < G) {
+      float M = mws[h];
+#pragma unroll
+      for (int w2 = 1; w2 < NW; ++w2) M = fmaxf(M, mws[w2 * G + h]);
+      const float fw = m[nt] == -INFINITY ? 0.f : exp2f(m[nt] - M);   // this warp's weight
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         int d0, d1;
@@ -1037,12 +1050,12 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
           o0 = fmaf(oacc[t][nt][1], 1.0f / tc::kLoScale, oacc[t][nt][0]);
           o1 = fmaf(oacc[t][nt][3], 1.0f / tc::kLoScale, oacc[t][nt][2]);
         }
-        ows[(w * G + h) * HD + d0] = fmaf(o0, sc, pbg);
-        ows[(w * G + h) * HD + d1] = fmaf(o1, sc, pbg);
+        ows[(w * G + h) * HD + d0] = fw * fmaf(o0, sc, pbg);
+        ows[(w * G + h) * HD + d1] = fw * fmaf(o1, sc, pbg);
       }
       if (gid == 0) {
-        mws[w * G + h] = m[nt];
-        lws[w * G + h] = lt;
+        lws[w * G + h] = fw * lt;
+        if (w == 0) Mh[h] = M;
       }
     }
   }
@@ -1051,21 +1064,16 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   const int64_t cidx = ((int64_t)b * a.n_kv_heads + kvh) * a.n_chunks + chunk;
   // cluster mode: the CTA's merged partial stays in its own shared memory,
   // o [G][HD] then (M, l) [G], after the warps' states
-  const uint32_t cpart = tc::smem_u32(smem) + (((uint32_t)(NW * G * HD + 2 * NW * G) * 4 + 15) & ~15u);
+  const uint32_t cpart = tc::smem_u32(smem) + (((uint32_t)(NW * G * HD + 2 * NW * G + G) * 4 + 15) & ~15u);
   const uint32_t cml = cpart + 4 * G * HD;
   for (int i = tid; i < G * HD; i += NW * 32) {
     const int h = i / HD, d = i - h * HD;
-    float M = mws[h];
-#pragma unroll
-    for (int w2 = 1; w2 < NW; ++w2) M = fmaxf(M, mws[w2 * G + h]);
+    const float M = Mh[h];
     float o = 0.f, ls = 0.f;
-    if (M != -INFINITY) {
 #pragma unroll
-      for (int w2 = 0; w2 < NW; ++w2) {
-        const float f = exp2f(mws[w2 * G + h] - M);
-        o = fmaf(f, ows[(w2 * G + h) * HD + d], o);
-        ls = fmaf(f, lws[w2 * G + h], ls);
-      }
+    for (int w2 = 0; w2 < NW; ++w2) {
+      o += ows[(w2 * G + h) * HD + d];
+      ls += lws[w2 * G + h];
     }
     if constexpr (CL) {
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(cpart + 4 * i), "f"(o) : "memory");
