@@ -38,6 +38,9 @@ Readings taken where the pages are silent (each also listed in the design doc):
   R6  attention scale defaults to 1/sqrt(head_dim) ([Shimmy] §2.3 comment);
       the shader line that divides by head_dim is read as garbled.
   R7  an empty context (L = 0) yields a zero output row.
+  R8  the unquantised "f16" KV type of [Kaiwu] finding 2 (f16 K + f16 V) stores
+      each element of the (rotated, fp32) row rounded once to fp16 (nearest,
+      ties to even), with no scale; its value is read back exactly.
 """
 from __future__ import annotations
 
@@ -196,7 +199,10 @@ def quantize_affine(x: np.ndarray, group: int, param: str):
 
 
 def quantize(kind: str, x: np.ndarray, group: int, param: str):
-    """(codes, scales, biases-or-None) for any quantised kind."""
+    """(codes, scales, biases-or-None) for any stored kind; "f16" (R8) keeps
+    the fp16-rounded values as its codes and has no scales."""
+    if kind == "f16":
+        return np.asarray(x, dtype=np.float32).astype(np.float16), None, None
     if kind == "sym4":
         c, s = quantize_sym(x, group, 4, param)
         return c, s, None
@@ -209,8 +215,10 @@ def quantize(kind: str, x: np.ndarray, group: int, param: str):
 
 
 def dequantize(codes: np.ndarray, scales: np.ndarray, biases, group: int) -> np.ndarray:
-    """x^ = scale * code (+ bias), in fp64."""
+    """x^ = scale * code (+ bias), in fp64; an unscaled kind (no scales) is its codes."""
     c = np.asarray(codes).astype(np.float64)
+    if scales is None:
+        return c
     lead, hd = c.shape[:-1], c.shape[-1]
     cg = c.reshape(*lead, hd // group, group)
     out = cg * np.asarray(scales, dtype=np.float64)[..., None]
@@ -299,10 +307,14 @@ def rotate_f64(x: np.ndarray, pos: int, head_dim: int, base: float, mode: str) -
 
 
 def code_bytes(kind: str, head_dim: int) -> int:
+    if kind == "f16":
+        return 2 * head_dim
     return head_dim if kind == "sym8" else head_dim // 2
 
 
 def param_row_bytes(kind: str, head_dim: int, group: int, param: str) -> int:
+    if kind == "f16":
+        return 0
     n_params = 2 if kind == "affine4" else 1
     return (head_dim // group) * n_params * PARAM_BYTES[param]
 
@@ -326,6 +338,9 @@ def _kv(spec: Spec, which: str):
 
 def pack_codes(kind: str, codes: np.ndarray) -> np.ndarray:
     """codes [..., hd] -> bytes [..., code_bytes]."""
+    if kind == "f16":
+        c = np.ascontiguousarray(codes, dtype="<f2")
+        return c.view(np.uint8).reshape(*c.shape[:-1], 2 * c.shape[-1])
     if kind == "sym8":
         return np.asarray(codes, dtype=np.int8).view(np.uint8)
     c = np.asarray(codes).astype(np.int16) & 0xF
@@ -335,6 +350,8 @@ def pack_codes(kind: str, codes: np.ndarray) -> np.ndarray:
 def unpack_codes(kind: str, raw: np.ndarray) -> np.ndarray:
     """bytes [..., code_bytes] -> codes [..., hd] (int16)."""
     raw = np.asarray(raw, dtype=np.uint8)
+    if kind == "f16":
+        return np.ascontiguousarray(raw).view("<f2")
     if kind == "sym8":
         return raw.view(np.int8).astype(np.int16)
     lo = (raw & 0xF).astype(np.int16)
@@ -370,6 +387,8 @@ def _bytes_to_param(raw: np.ndarray, param: str) -> np.ndarray:
 
 
 def _params_row(kind, scales, biases, param):
+    if scales is None:   # an unscaled kind: no parameter bytes
+        return np.zeros(0, np.uint8)
     if kind == "affine4":
         inter = np.stack([scales, biases], axis=-1).reshape(
             *scales.shape[:-1], 2 * scales.shape[-1])
@@ -451,6 +470,8 @@ def read_tokens(spec: Spec, which: str, pool: np.ndarray, block_table_row,
     heads = np.arange(spec.n_kv_heads)[None, :]
     oc, op, cb, pb = _slot_offsets(spec, which, pg[:, None], sl[:, None], heads)
     codes = unpack_codes(kind, pool[oc[..., None] + np.arange(cb)])
+    if pb == 0:
+        return codes, None, None
     prm = _bytes_to_param(pool[op[..., None] + np.arange(pb)], par)
     if kind == "affine4":
         return codes, prm[..., 0::2], prm[..., 1::2]

@@ -325,7 +325,7 @@ def _small_spec(**kw):
     return O.Spec(**base)
 
 
-@pytest.mark.parametrize("kinds", [("sym4", "sym4"), ("sym8", "sym4"), ("affine4", "affine4")])
+@pytest.mark.parametrize("kinds", [("sym4", "sym4"), ("sym8", "sym4"), ("affine4", "affine4"), ("f16", "f16")])
 def test_paged_equals_contiguous(kinds):
     kk, vk = kinds
     par = "bf16" if kk == "affine4" else "f16"
@@ -380,6 +380,35 @@ def test_page_layout_offsets():
     other = pools["k"][3 * 8704 + 1088 * 5: 3 * 8704 + 1088 * 6]
     assert np.count_nonzero(other[:1024]) == 0
     assert np.frombuffer(other[1024 + 20: 1024 + 24].tobytes(), "<f4")[0] == np.float32(1e-8)
+
+
+def test_f16_kv_layout_and_brute_force_attention():
+    """The unquantised f16 KV type (reading R8, [Kaiwu] finding 2 "f16+f16"):
+    a sub-block is 16 rows of 2 * head_dim bytes, each row the fp16 rounding of
+    its elements with no scale; decode equals brute-force softmax attention
+    over those fp16 values."""
+    spec = O.Spec(n_heads=4, n_kv_heads=2, head_dim=32, page_size=16, k_kind="f16", v_kind="f16",
+                  k_group=32, v_group=32, k_param="f32", v_param="f32", act="f32", rope="none")
+    assert O.code_bytes("f16", 32) == 64 and O.param_row_bytes("f16", 32, 32, "f32") == 0
+    assert O.page_bytes(spec, "k") == 2 * 16 * 64
+    rng = np.random.default_rng(7)
+    L = 21
+    k = rng.standard_normal((L, 2, 32)).astype(np.float32) * 3
+    v = rng.standard_normal((L, 2, 32)).astype(np.float32)
+    bt = np.array([[4, 1]], np.int32)
+    pools = {w: np.zeros(5 * O.page_bytes(spec, w), np.uint8) for w in ("k", "v")}
+    O.append(spec, pools, k, v, np.zeros(L, np.int64), np.arange(L), bt)
+    # token 17 sits in page bt[0][1] = 1, slot 1, kv head 1
+    off = 1 * O.page_bytes(spec, "k") + 1 * 16 * 64 + 1 * 64
+    assert pools["k"][off:off + 64].tobytes() == k[17, 1].astype("<f2").tobytes()
+    q = rng.standard_normal((1, 4, 32))
+    got = O.decode(spec, q, pools, bt, np.array([L]))
+    K16 = k.astype(np.float16).astype(np.float64)
+    V16 = v.astype(np.float16).astype(np.float64)
+    for h in range(4):
+        ref = _brute_attend(q[0, h].tolist(), K16[:, h // 2].tolist(), V16[:, h // 2].tolist(),
+                            1.0 / np.sqrt(32.0))
+        assert np.allclose(got[0, h], ref, rtol=1e-12, atol=1e-12)
 
 
 def test_ring_equals_explicit_window():
