@@ -45,6 +45,9 @@ MODELS = {
     "contbatch": [("contbatch", 1, False)],                    # 1.16 GB per layer already > L2
     "long_mixed": [("long_mixed", 4, False)],
     "gemma_mix": [("gemma_mix", 25, True), ("gemma_mix", 5, False)],   # 25 window + 5 global
+    # the unquantised f16 K/V the pages compare with (8K and 64K)
+    "llama8b_f16": [("llama8b_f16", 32, False)],
+    "long_f16": [("long_f16", 4, False)],
 }
 
 

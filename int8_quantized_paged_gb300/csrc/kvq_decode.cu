@@ -36,11 +36,19 @@ static constexpr int kMaxChunks = 8192;
 // Whether the tensor-core kernel takes this config (and is not switched off):
 // power-of-two groups of at least 32 elements, a head_dim/G shape with an
 // instantiation, and one stored type for the K and V scales.
+// Scale groups per head of the tensor-core kernel (1 for unquantised f16).
+static int tc_ng(const kvq_config& c) { return c.k_dtype == KVQ_F16_KV ? 1 : c.head_dim / c.k_group; }
+
+// f16 K/V have only the tensor-core kernel (head_dim 64 and 128).
 static bool tc_enabled(const kvq_config& c) {
   static int forced = -1;
   if (forced < 0) {
     const char* e = std::getenv("KVQ_DECODE_IMPL");
     forced = (e && std::strcmp(e, "simt") == 0) ? 0 : 1;
+  }
+  if (c.k_dtype == KVQ_F16_KV) {
+    const int G = c.n_heads / c.n_kv_heads;
+    return c.head_dim <= 128 && tc_has_shape(c.head_dim, G > 4 ? 2 : 1, 1);
   }
   if (!forced) return false;
   const bool pow2 = (c.k_group & (c.k_group - 1)) == 0 && (c.v_group & (c.v_group - 1)) == 0;
@@ -88,6 +96,7 @@ static int max_active_clusters(TcLaunch fn, const TcArgs& t, int hd, int nt, int
 
 // The tensor-core launcher of a config's K/V kinds and scale type.
 static TcLaunch tc_launcher(const kvq_config& c) {
+  if (c.k_dtype == KVQ_F16_KV) return launch_tc_h16;   // no scales: one instantiation
   static const TcLaunch table[4][3] = {
       {launch_tc_s4s4_f32, launch_tc_s4s4_f16, launch_tc_s4s4_bf16},
       {launch_tc_s8s8_f32, launch_tc_s8s8_f16, launch_tc_s8s8_bf16},
@@ -104,8 +113,8 @@ static TcLaunch tc_launcher(const kvq_config& c) {
 // Bytes of one warp's ring of page slots.
 static size_t tc_ring_bytes(const kvq_config& c) {
   const int G = c.n_heads / c.n_kv_heads;
-  return (size_t)tc_depth(c.head_dim, G > 4 ? 2 : 1) *
-         tc_slot_bytes(c.k_dtype, c.v_dtype, c.head_dim, c.head_dim / c.k_group, c.k_param_dtype);
+  return (size_t)tc_depth(c.head_dim, G > 4 ? 2 : 1, c.k_dtype) *
+         tc_slot_bytes(c.k_dtype, c.v_dtype, c.head_dim, tc_ng(c), c.k_param_dtype);
 }
 
 // The cluster mode: a few sequences, each short enough that one cluster of
@@ -150,7 +159,7 @@ static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens,
     q.smem = smem;
     q.warps = kClusterWarps;
     q.cluster = (int)nc;
-    if (max_active_clusters(fn, none, hd, nt, hd / c.k_group, q) >= batch * c.n_kv_heads) {
+    if (max_active_clusters(fn, none, hd, nt, tc_ng(c), q) >= batch * c.n_kv_heads) {
       *lc = q;
       *cb_out = (int)cb;
       return true;
@@ -162,7 +171,7 @@ static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens,
 // CTAs of the tensor-core kernel resident per SM (its launch bounds).
 static int tc_resident(const kvq_config& c) {
   const int G = c.n_heads / c.n_kv_heads;
-  return tc_min_blocks(c.head_dim, G > 4 ? 2 : 1);
+  return tc_min_blocks(c.head_dim, G > 4 ? 2 : 1, c.k_dtype);
 }
 
 // Chunking and workspace layout of one decode call.  The workspace holds, in
@@ -324,7 +333,7 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     t.cluster = 0;
     const int nt = G > 4 ? 2 : 1;
     const int hd = cfg->head_dim;
-    const int ng = hd / cfg->k_group;   // scale groups per head (K and V alike)
+    const int ng = tc_ng(*cfg);   // scale groups per head (K and V alike)
     const int pt = cfg->k_param_dtype;
     if (t.kp_bytes != tc_scale_bytes(k, ng, pt) || t.vp_bytes != tc_scale_bytes(v, ng, pt))
       return fail(KVQ_ERR_UNSUPPORTED, "scale rows do not match the tensor-core kernel's slots");
@@ -362,6 +371,8 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     return fn(t, hd, nt, ng, lc);
   }
 
+  if (k == KVQ_F16_KV)
+    return fail(KVQ_ERR_UNSUPPORTED, "f16 K/V: no tensor-core kernel for head_dim %d and G %d", cfg->head_dim, G);
   const dim3 grid(w.n_chunks, cfg->n_kv_heads, batch);
   kvq_status st;
   if (k == KVQ_SYM_INT4 && v == KVQ_SYM_INT4) st = launch_decode_s4s4(a, cfg->head_dim, G, grid, stream);
@@ -422,7 +433,7 @@ extern "C" int32_t kvq_decode_cluster_ctas(const kvq_config* cfg, int32_t batch,
   TcLaunchCfg lc{};
   int cb = 0;
   const bool on = pick_cluster(*cfg, batch, max_tokens, window, tc_launcher(*cfg), tc_ring_bytes(*cfg),
-                               tc_pre_bytes(cfg->head_dim, G > 4 ? 2 : 1, cfg->head_dim / cfg->k_group), &lc, &cb);
+                               tc_pre_bytes(cfg->head_dim, G > 4 ? 2 : 1, tc_ng(*cfg)), &lc, &cb);
   return on ? lc.cluster : 0;
 }
 

@@ -80,8 +80,14 @@ constexpr float kWScale = 128.0f;   // w is held x 2^7 (w <= 2^8 * 2^7 < 65504)
 constexpr float kLazyMax = 8.0f;    // raise the running max only past +2^8
 
 // Pages in flight per warp, and CTAs per SM (the launch bounds), by shape.
-__host__ __device__ constexpr int tc_depth(int hd, int nt) { return (hd == 256 || nt == 2) ? 3 : 4; }
-__host__ __device__ constexpr int tc_min_blocks(int hd, int nt) { return hd <= 128 ? (nt == 1 ? 5 : 4) : 3; }
+// f16 K/V pages are 4 times larger: 2 in flight per warp at hd 128 (4 at hd 64),
+// 3 CTAs per SM.
+__host__ __device__ constexpr int tc_depth(int hd, int nt, int kind = KVQ_SYM_INT4) {
+  return kind == KVQ_F16_KV ? (hd == 128 ? 2 : 4) : ((hd == 256 || nt == 2) ? 3 : 4);
+}
+__host__ __device__ constexpr int tc_min_blocks(int hd, int nt, int kind = KVQ_SYM_INT4) {
+  return kind == KVQ_F16_KV ? 3 : (hd <= 128 ? (nt == 1 ? 5 : 4) : 3);
+}
 // Shapes with a cluster-mode instantiation (one 8-column tile: G <= 4), and
 // the cluster-mode CTAs resident per SM.
 __host__ __device__ constexpr bool tc_cluster_shape(int hd, int nt) { return nt == 1; }
@@ -92,10 +98,10 @@ __host__ __device__ constexpr int tc_qfrag_bytes(int hd, int nt) { return nt * h
 // Shared memory after the page rings: the query fragments, the RoPE row of
 // the query's position (hd / 2 cos/sin pairs), the affine-K per-group q sums
 // ([nt][ng][4 heads]) and, for a fused append, the new K and V rows (up to
-// fp32) with the RoPE row of their position, then their quantized rows (codes
-// up to 8-bit, parameter rows up to 64 bytes).
+// fp32) with the RoPE row of their position, then their quantized rows (code
+// rows up to 2 hd bytes (f16), parameter rows up to 64 bytes).
 __host__ __device__ constexpr int tc_pre_bytes(int hd, int nt, int ng) {
-  return tc_qfrag_bytes(hd, nt) + 4 * hd + 16 * nt * ng + 14 * hd + 128;
+  return tc_qfrag_bytes(hd, nt) + 4 * hd + 16 * nt * ng + 16 * hd + 128;
 }
 
 // Fused append: quantizes the staged row (K rotated at its position) exactly
@@ -143,27 +149,37 @@ __device__ __forceinline__ float ld_param(uint32_t addr) {
 
 // Scale (and bias) bytes of one page of one kv head with ng groups per head.
 __host__ __device__ constexpr int tc_scale_bytes(int kind, int ng, int pt) {
-  return 16 * ng * (kind == KVQ_AFFINE_INT4 ? 2 : 1) * (pt == KVQ_F32 ? 4 : 2);
+  return kind == KVQ_F16_KV ? 0 : 16 * ng * (kind == KVQ_AFFINE_INT4 ? 2 : 1) * (pt == KVQ_F32 ? 4 : 2);
+}
+// Bytes of one code row of a kind (hd elements).
+__host__ __device__ constexpr int tc_row_bytes(int kind, int hd) {
+  return kind == KVQ_F16_KV ? 2 * hd : (kind == KVQ_SYM_INT8 ? hd : hd / 2);
 }
 __host__ __device__ constexpr int tc_slot_bytes(int kk, int vk, int hd, int ng, int pt) {
-  return 16 * (kk == KVQ_SYM_INT8 ? hd : hd / 2) + 16 * (vk == KVQ_SYM_INT8 ? hd : hd / 2) +
-         tc_scale_bytes(kk, ng, pt) + tc_scale_bytes(vk, ng, pt);
+  return 16 * tc_row_bytes(kk, hd) + 16 * tc_row_bytes(vk, hd) + tc_scale_bytes(kk, ng, pt) +
+         tc_scale_bytes(vk, ng, pt);
 }
 
 // N consecutive activation elements (f32 / f16 / bf16) from element `off` of
 // `p`, with vector loads; `off` is a multiple of N and the base 16-byte aligned.
 template <int N>
 __device__ __forceinline__ void load_run(const void* p, int act, int64_t off, float (&v)[N]) {
-  static_assert(N == 4 || N == 8, "run");
+  static_assert(N == 2 || N == 4 || N == 8, "run");
   if (act == KVQ_F32) {
-    const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(p) + off);
+    if constexpr (N == 2) {
+      const float2 x = *reinterpret_cast<const float2*>(static_cast<const float*>(p) + off);
+      v[0] = x.x;
+      v[1] = x.y;
+    } else {
+      const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(p) + off);
 #pragma unroll
-    for (int i = 0; i < N / 4; ++i) {
-      const float4 x = s[i];
-      v[4 * i] = x.x;
-      v[4 * i + 1] = x.y;
-      v[4 * i + 2] = x.z;
-      v[4 * i + 3] = x.w;
+      for (int i = 0; i < N / 4; ++i) {
+        const float4 x = s[i];
+        v[4 * i] = x.x;
+        v[4 * i + 1] = x.y;
+        v[4 * i + 2] = x.z;
+        v[4 * i + 3] = x.w;
+      }
     }
   } else {
     uint32_t u[N / 2];
@@ -171,9 +187,11 @@ __device__ __forceinline__ void load_run(const void* p, int act, int64_t off, fl
     if constexpr (N == 8) {
       const uint4 x = *reinterpret_cast<const uint4*>(s);
       u[0] = x.x; u[1] = x.y; u[2] = x.z; u[3] = x.w;
-    } else {
+    } else if constexpr (N == 4) {
       const uint2 x = *reinterpret_cast<const uint2*>(s);
       u[0] = x.x; u[1] = x.y;
+    } else {
+      u[0] = *reinterpret_cast<const uint32_t*>(s);
     }
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) {
@@ -217,22 +235,26 @@ __device__ __forceinline__ float hilo_part_unscaled(float x, int part) {
 // (sequence, kv head) one cluster of A.cluster CTAs); else kWarps warps.
 template <int KK, int VK, int HD, int NT, int NG, int PT, bool CL>
 __global__ void __launch_bounds__(32 * (CL ? kClusterWarps : kWarps),
-                                   CL ? tc_cluster_min_blocks(HD) : tc_min_blocks(HD, NT))
+                                   CL ? tc_cluster_min_blocks(HD) : tc_min_blocks(HD, NT, KK))
 decode_tc_kernel(const __grid_constant__ TcArgs A) {
   constexpr int P = 16;
   constexpr int NW = CL ? kClusterWarps : kWarps;
-  constexpr int D = tc_depth(HD, NT);           // pages in flight per warp
+  constexpr int D = tc_depth(HD, NT, KK);       // pages in flight per warp
   constexpr bool K8 = KK == KVQ_SYM_INT8, V8 = VK == KVQ_SYM_INT8;
   constexpr bool KAFF = KK == KVQ_AFFINE_INT4, VAFF = VK == KVQ_AFFINE_INT4;
-  constexpr int KRB = K8 ? HD : HD / 2;          // K code row bytes
-  constexpr int VRB = V8 ? HD : HD / 2;
+  // F16: unquantised fp16 K and V (no scales): the ldmatrix fragments are the
+  // MMA operands as they are, and the stored scales below read as 1
+  constexpr bool F16 = KK == KVQ_F16_KV;
+  static_assert(F16 == (VK == KVQ_F16_KV), "f16 K goes with f16 V");
+  constexpr int KRB = tc_row_bytes(KK, HD);      // K code row bytes
+  constexpr int VRB = tc_row_bytes(VK, HD);
   constexpr int KCH = KRB / 16;                  // 16-byte chunks per K row
   constexpr int VCH = VRB / 16;
-  constexpr int KDC = K8 ? 16 : 32;              // dims per K chunk
-  constexpr int VDC = V8 ? 16 : 32;
-  constexpr int KSTEPS = K8 ? KCH : 2 * KCH;     // Q.K k-steps
+  constexpr int KDC = F16 ? 8 : (K8 ? 16 : 32);  // dims per K chunk
+  constexpr int VDC = F16 ? 8 : (V8 ? 16 : 32);
+  constexpr int KSTEPS = F16 ? KCH / 2 : (K8 ? KCH : 2 * KCH);   // Q.K k-steps
   constexpr int MT = HD / 16;                    // P.V m-tiles
-  constexpr int RUN = K8 ? 4 : 8;                // contiguous q dims a lane holds per K chunk
+  constexpr int RUN = F16 ? 2 : (K8 ? 4 : 8);    // contiguous q dims a lane holds per K chunk
   constexpr int PB = PT == KVQ_F32 ? 4 : 2;      // bytes of a stored scale
   constexpr bool ONEG = NG == 1;
   constexpr int GS = HD / NG;                    // dims per scale group
@@ -326,15 +348,19 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   constexpr int NCP_ALL = cmin(KSUB, VSUB) / 16;                       // copies every lane makes
   const int n_sub = vlane ? VSUB : KSUB;
   const int cnt = n_sub > hl ? (n_sub - hl + 15) / 16 : 0;             // this lane's copies
-  uint32_t cp_dst[NCP];
+  // f16 rows: 16 copies a lane of rows with no scales, the destinations
+  // computed as they go (keeping them would take 16 registers)
+  constexpr int NCPR = F16 ? 1 : NCP;
+  uint32_t cp_dst[NCPR];
 #pragma unroll
-  for (int m = 0; m < NCP; ++m) {
+  for (int m = 0; m < NCPR; ++m) {
     const int j = hl + 16 * m;
     uint32_t d;
     if (!vlane) d = j < KC / 16 ? swz<KRB>(j / KCH, j % KCH) : KC + VC + 16 * (j - KC / 16);
     else d = j < VC / 16 ? KC + swz<VRB>(j / VCH, j % VCH) : KC + VC + KPMAX + 16 * (j - VC / 16);
     cp_dst[m] = wring + d;
   }
+  const uint32_t lane_sub = wring + (vlane ? KC : 0);   // f16: this lane's sub-block in slot 0
   const int ring = a.ring_rows, npp = a.n_pool_pages;
   auto page_of = [&](int k) -> int {   // page id of this warp's k-th page (k < n_local)
     const int blk = cb0 + w + NW * k;
@@ -461,7 +487,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       const uint4 x = *reinterpret_cast<const uint4*>(smem + qv_off + 16 * (lane - 16));
       *reinterpret_cast<uint4*>(slot + KC + swz<VRB>(r, lane - 16)) = x;
     }
-    constexpr int kprb_ = NG * (KAFF ? 2 : 1) * PB, vprb_ = NG * (VAFF ? 2 : 1) * PB;
+    constexpr int kprb_ = F16 ? 0 : NG * (KAFF ? 2 : 1) * PB, vprb_ = F16 ? 0 : NG * (VAFF ? 2 : 1) * PB;
     for (int j = lane; j < kprb_; j += 32) slot[KC + VC + r * kprb_ + j] = smem[qkp_off + j];
     for (int j = lane; j < vprb_; j += 32) slot[KC + VC + KPMAX + r * vprb_ + j] = smem[qvp_off + j];
   };
@@ -474,11 +500,21 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     if (pg < 0) return;
     const uint8_t* src = pool_lane + pg * page_lane;
     const uint32_t so = s * SLOT;
+    if constexpr (F16) {   // K and V sub-blocks alike: KSUB chunks, rows of KCH chunks
 #pragma unroll
-    for (int m = 0; m < NCP; ++m)
-      if (m < NCP_ALL || m < cnt)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(cp_dst[m] + so), "l"(src + 256 * m)
+      for (int m = 0; m < KSUB / 16; ++m) {
+        const int j = hl + 16 * m;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(lane_sub + so + swz<KRB>(j / KCH, j % KCH)),
+                     "l"(src + 256 * m)
                      : "memory");
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < NCP; ++m)
+        if (m < NCP_ALL || m < cnt)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(cp_dst[m] + so), "l"(src + 256 * m)
+                       : "memory");
+    }
   };
 #pragma unroll
   for (int k = 0; k < D; ++k) {
@@ -531,6 +567,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     // (p = 1 meets 16 * code, so q / 16):
     //   b0 = q at dims KDC*c + 8tig + p + {0, 4},  b1 = dims + {2, 6}
     // 8-bit K chunk c:  b0 = dims 16c + 4tig + {0, 2},  b1 = dims + {1, 3}
+    // f16 K k-step s (chunks 2s, 2s+1 of 8 dims): b0 = dims 16s + 2tig + {0, 1},
+    // b1 = dims 16s + 8 + 2tig + {0, 1}
     // The part: high or low by the column's parity (NT = 1) or by the pass
     // (MRG, where the low part is not scaled up: both passes add into one
     // accumulator).
@@ -541,7 +579,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       uint32_t qb[KSTEPS][2];
 #pragma unroll
       for (int c = 0; c < KCH; ++c) {
-        if constexpr (K8) {
+        if constexpr (F16) {
+          qb[c / 2][c & 1] = tc::pack_half2(qp(qv[0][c][0]), qp(qv[0][c][1]));
+        } else if constexpr (K8) {
           qb[c][0] = tc::pack_half2(qp(qv[0][c][0]), qp(qv[0][c][2]));
           qb[c][1] = tc::pack_half2(qp(qv[0][c][1]), qp(qv[0][c][3]));
         } else {
@@ -613,8 +653,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   // ---- per-lane constants of the main loop
   // parameter rows: per group a scale (and an affine bias) of PB bytes; the
   // host checks that the pools' rows have this layout
-  constexpr int kstep = (KAFF ? 2 : 1) * PB, vstep = (VAFF ? 2 : 1) * PB;   // bytes per group in a row
-  constexpr int kprb = NG * kstep, vprb = NG * vstep;                        // bytes per row
+  constexpr int kstep = F16 ? 0 : (KAFF ? 2 : 1) * PB, vstep = F16 ? 0 : (VAFF ? 2 : 1) * PB;   // per group
+  constexpr int kprb = NG * kstep, vprb = NG * vstep;                                          // per row
   const int mi = lane >> 3;
   const int trow = 8 * (mi & 1) + (lane & 7);    // token row this lane addresses in ldmatrix
   int kls[KCH / 2], vls[VCH / 2];
@@ -683,7 +723,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const uint32_t pr = kp + (gid + 8 * j) * kprb + g * kstep;
-        const float ks = ld_param<PT>(pr) * (1.0f / kQScale);
+        const float ks = F16 ? 1.0f / kQScale : ld_param<PT>(pr) * (1.0f / kQScale);
         float kb = 0.f;
         if constexpr (KAFF) kb = ld_param<PT>(pr + PB);
 #pragma unroll
@@ -711,6 +751,18 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     for (int c2 = 0; c2 < KCH / 2; ++c2) {
       uint32_t r[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
       tc::ldsm_x4(kc + kls[c2], r);
+      if constexpr (F16) {
+        // k-step c2: the fragment as loaded, B = words 2 (c2 % 2), +1 of uint4 c2 / 2
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          uint32_t b0, b1;
+          asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                       : "=r"(b0), "=r"(b1)
+                       : "r"(qfs + ((nt * (KSTEPS / 2) + c2 / 2) * 32 + lane) * 16 + (c2 & 1) * 8));
+          tc::mma_16816(sacc[nt], r, b0, b1);
+        }
+        continue;
+      }
       // query fragments of chunks 2c2, 2c2+1: uint4s (K8: one for both, 4-bit: one each)
       uint32_t qf[NT][2][4];
 #pragma unroll
@@ -807,7 +859,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const uint32_t pr = vp + (gid + 8 * j) * vprb + g * vstep;
-        vs[j] = ld_param<PT>(pr);
+        vs[j] = F16 ? 1.0f : ld_param<PT>(pr);
         if constexpr (VAFF) vb[j] = ld_param<PT>(pr + PB);
         if (edge) {
           const int t = tb + gid + 8 * j;
@@ -888,6 +940,13 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     for (int c2 = 0; c2 < VCH / 2; ++c2) {
       uint32_t y[4];   // (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
       tc::ldsm_x4_trans(vc + vls[c2], y);
+      if constexpr (F16) {
+        // m-tile c2 (dims of chunks 2c2, 2c2+1): A = V^T as loaded, rows dims
+        const uint32_t av[4] = {y[0], y[2], y[1], y[3]};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) tc::mma_16816(oacc[c2][MRG ? 0 : nt], av, bw[nt][0], bw[nt][1]);
+        continue;
+      }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * c2 + cc;
@@ -1021,7 +1080,11 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       for (int t = 0; t < MT; ++t) {
         int d0, d1;
         float f;
-        if constexpr (V8) {
+        if constexpr (F16) {   // rows gid / gid+8 of tile t: dims 16t + gid, + 8
+          d0 = 16 * t + gid;
+          d1 = d0 + 8;
+          f = 1.0f;
+        } else if constexpr (V8) {
           d0 = 16 * t + 2 * gid;
           d1 = d0 + 1;
           f = 1.0f;
@@ -1307,6 +1370,10 @@ kvq_status launch_tc_one(const TcArgs& t, const TcLaunchCfg& lc) {
   return KVQ_OK;
 }
 
+// The shapes a K kind is instantiated for: f16 K/V at head_dim 64 and 128
+// with one (unused) scale group; the quantised kinds at every shape below.
+constexpr bool tc_kind_shape(int kk, int hd, int ng) { return kk != KVQ_F16_KV || (hd <= 128 && ng == 1); }
+
 // Shapes with a tensor-core instantiation: head_dim 64 and 256 with G <= 4,
 // head_dim 128 with any G; ng = head_dim / group scale groups per head, with
 // groups of at least 32 elements.
@@ -1318,12 +1385,13 @@ inline bool tc_has_shape(int head_dim, int nt, int ng) {
 template <int KK, int VK, int PT>
 kvq_status launch_tc_pt(const TcArgs& t, int head_dim, int nt, int ng, const TcLaunchCfg& lc) {
 #define KVQ_TC(HD_, NT_, NG_)                                                                      \
-  if (head_dim == HD_ && nt == NT_ && ng == NG_) {                                                 \
-    if constexpr (tc_cluster_shape(HD_, NT_))                                                       \
-      if (lc.cluster > 0) return launch_tc_one<KK, VK, HD_, NT_, NG_, PT, true>(t, lc);            \
-    if (lc.cluster > 0) return fail(KVQ_ERR_UNSUPPORTED, "no cluster-mode kernel for this shape");  \
-    return launch_tc_one<KK, VK, HD_, NT_, NG_, PT, false>(t, lc);                                 \
-  }
+  if constexpr (tc_kind_shape(KK, HD_, NG_))                                                       \
+    if (head_dim == HD_ && nt == NT_ && ng == NG_) {                                               \
+      if constexpr (tc_cluster_shape(HD_, NT_))                                                     \
+        if (lc.cluster > 0) return launch_tc_one<KK, VK, HD_, NT_, NG_, PT, true>(t, lc);          \
+      if (lc.cluster > 0) return fail(KVQ_ERR_UNSUPPORTED, "no cluster-mode kernel for this shape"); \
+      return launch_tc_one<KK, VK, HD_, NT_, NG_, PT, false>(t, lc);                               \
+    }
   KVQ_TC(64, 1, 1)
   KVQ_TC(64, 1, 2)
   KVQ_TC(128, 1, 1)
@@ -1355,6 +1423,7 @@ KVQ_TC_DECLARE(launch_tc_s8s4_bf16)
 KVQ_TC_DECLARE(launch_tc_a4a4_f32)
 KVQ_TC_DECLARE(launch_tc_a4a4_f16)
 KVQ_TC_DECLARE(launch_tc_a4a4_bf16)
+KVQ_TC_DECLARE(launch_tc_h16)
 #undef KVQ_TC_DECLARE
 
 }  // namespace kvq

@@ -82,11 +82,17 @@ kvq_status check_kernel_config(const kvq_config* c) {
   const bool pair_ok = (k == KVQ_SYM_INT4 && v == KVQ_SYM_INT4) ||
                        (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT8) ||
                        (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT4) ||
-                       (k == KVQ_AFFINE_INT4 && v == KVQ_AFFINE_INT4);
+                       (k == KVQ_AFFINE_INT4 && v == KVQ_AFFINE_INT4) ||
+                       (k == KVQ_F16_KV && v == KVQ_F16_KV);
   if (!pair_ok)
     return fail(KVQ_ERR_UNSUPPORTED,
                 "K/V dtype pair (%d, %d); kernels exist for sym4/sym4, sym8/sym8, sym8/sym4, "
-                "affine4/affine4", k, v);
+                "affine4/affine4, f16/f16", k, v);
+  if (k == KVQ_F16_KV) {   // unquantised: no groups; the tensor-core kernel only
+    if (c->head_dim == 256)
+      return fail(KVQ_ERR_UNSUPPORTED, "f16 K/V: kernels exist for head_dim 64 and 128");
+    return KVQ_OK;
+  }
   if (c->k_group % 16 != 0 || c->v_group % 16 != 0)
     return fail(KVQ_ERR_UNSUPPORTED, "groups (%d, %d) must be multiples of 16", c->k_group,
                 c->v_group);
@@ -98,9 +104,16 @@ PoolLayout pool_layout(const kvq_config& c, int which) {
   L.kind = which ? c.v_dtype : c.k_dtype;
   L.group = which ? c.v_group : c.k_group;
   L.param = which ? c.v_param_dtype : c.k_param_dtype;
-  L.n_groups = c.head_dim / L.group;
-  L.n_params = L.kind == KVQ_AFFINE_INT4 ? 2 : 1;
-  L.code_bytes = L.kind == KVQ_SYM_INT8 ? c.head_dim : c.head_dim / 2;
+  if (L.kind == KVQ_F16_KV) {   // unquantised: fp16 rows, no parameters
+    L.group = c.head_dim;
+    L.n_groups = 1;
+    L.n_params = 0;
+    L.code_bytes = 2 * c.head_dim;
+  } else {
+    L.n_groups = c.head_dim / L.group;
+    L.n_params = L.kind == KVQ_AFFINE_INT4 ? 2 : 1;
+    L.code_bytes = L.kind == KVQ_SYM_INT8 ? c.head_dim : c.head_dim / 2;
+  }
   L.param_row_bytes = L.n_groups * L.n_params * param_bytes(L.param);
   L.sub_bytes = c.page_size * (L.code_bytes + L.param_row_bytes);
   L.page_bytes = (int64_t)c.n_kv_heads * L.sub_bytes;

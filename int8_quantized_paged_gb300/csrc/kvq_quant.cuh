@@ -61,7 +61,7 @@ __device__ __forceinline__ float rint_quotient(float x, float s, float r) {
 // The lane's quantized row piece: its packed code bytes (DPL/2 for 4-bit
 // kinds, DPL for 8-bit, little-endian in w) and its group's parameters.
 struct RowCodes {
-  uint2 w;        // packed codes, low bytes first
+  uint4 w;        // packed codes, low bytes first
   int nbytes;     // bytes of w that hold codes
   float scale;    // the group's stored scale (rounded to its type)
   float bias;     // affine: the group's stored bias
@@ -76,6 +76,17 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
   r.group = lane / lpg;
   r.leader = lane % lpg == 0;
   r.bias = 0.f;
+  if (L.kind == KVQ_F16_KV) {   // unquantised: the fp16 rounding of each element, no parameters
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < DPL; ++j)
+      w[j / 2] |= (uint32_t)__half_as_ushort(__float2half_rn(x[j])) << (16 * (j % 2));
+    r.w = make_uint4(w[0], w[1], w[2], w[3]);
+    r.nbytes = 2 * DPL;
+    r.scale = 1.f;
+    r.leader = false;
+    return r;
+  }
   int c[DPL];
   if (L.kind == KVQ_AFFINE_INT4) {
     float mn = x[0], mx = x[0];
@@ -123,7 +134,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
     for (int j = 0; j < DPL; ++j) w[0] |= ((uint32_t)c[j] & 0xFu) << (4 * j);
     r.nbytes = DPL / 2;
   }
-  r.w = make_uint2(w[0], w[1]);
+  r.w = make_uint4(w[0], w[1], 0u, 0u);
   return r;
 }
 
@@ -135,16 +146,18 @@ __device__ __forceinline__ int param_bias_offset(const PoolLayout& L, int g) {
   return (2 * g + 1) * param_bytes(L.param);
 }
 
-// Writes `nbytes` (1, 2, 4 or 8) low bytes of w at p, which is aligned to nbytes.
-__device__ __forceinline__ void store_code_bytes(uint8_t* p, uint2 w, int nbytes) {
+// Writes `nbytes` (1, 2, 4, 8 or 16) low bytes of w at p, which is aligned to nbytes.
+__device__ __forceinline__ void store_code_bytes(uint8_t* p, uint4 w, int nbytes) {
   if (nbytes == 1) {
     *p = (uint8_t)w.x;
   } else if (nbytes == 2) {
     *reinterpret_cast<unsigned short*>(p) = (unsigned short)w.x;
   } else if (nbytes == 4) {
     *reinterpret_cast<uint32_t*>(p) = w.x;
+  } else if (nbytes == 8) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(w.x, w.y);
   } else {
-    *reinterpret_cast<uint2*>(p) = w;
+    *reinterpret_cast<uint4*>(p) = w;
   }
 }
 

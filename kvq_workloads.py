@@ -26,13 +26,17 @@ from a seeded numpy ``Generator``):
                   K symmetric INT8 group 32 and V symmetric INT4 group 32, both
                   with fp16 scales; K/V ~N(0,1) with a seeded 1 % of elements
                   multiplied by 8.
+* ``llama8b_f16``, ``long_f16`` -- the ``llama8b`` and ``long_mixed`` shapes
+                  with unquantised f16 K and V (the "f16+f16" KV type the
+                  pages compare the quantised ones with).
 """
 from __future__ import annotations
 
 import numpy as np
 
 # Plain descriptions of each workload.  Strings name the codec kinds:
-#   "sym4"  symmetric 4-bit, "sym8" symmetric 8-bit, "affine4" affine 4-bit.
+#   "sym4"  symmetric 4-bit, "sym8" symmetric 8-bit, "affine4" affine 4-bit,
+#   "f16"   unquantised f16.
 WORKLOADS: dict[str, dict] = {
     "tiny": dict(
         index=0, batch=1, n_heads=4, n_kv_heads=2, head_dim=64, ctx=256,
@@ -65,6 +69,10 @@ WORKLOADS: dict[str, dict] = {
         rope="normal", rope_base=500000.0, outlier_frac=0.01,
         window=0, ring_rows=0),
 }
+
+WORKLOADS["llama8b_f16"] = dict(WORKLOADS["llama8b"], index=5, k_kind="f16", v_kind="f16")
+WORKLOADS["long_f16"] = dict(WORKLOADS["long_mixed"], index=6, k_kind="f16", v_kind="f16", k_group=128,
+                             v_group=128, k_param="f32", v_param="f32")
 
 ACT_NUMPY = {"f32": np.float32, "f16": np.float16}
 

@@ -107,9 +107,11 @@ def test_validate_config():
         (dict(k_group=48), kvq.ERR_INVALID_ARG),          # does not divide 128
         (dict(k_group=8, v_group=8), kvq.ERR_UNSUPPORTED),  # not a multiple of 16
         (dict(k_kind="sym4", v_kind="sym8"), kvq.ERR_UNSUPPORTED),
-        (dict(k_kind="f16", v_kind="f16"), kvq.ERR_UNSUPPORTED),
+        (dict(k_kind="f16", v_kind="f16", head_dim=256, k_group=256, v_group=256), kvq.ERR_UNSUPPORTED),
+        (dict(k_kind="f16", v_kind="sym4"), kvq.ERR_UNSUPPORTED),
         (dict(rope_base=-1.0), kvq.ERR_INVALID_ARG),
     ]
+    kvq.validate_config(_cfg(wl.workload("llama8b_f16")))   # unquantised f16 K/V at head_dim 128
     for over, want in bad:
         w = dict(wl.workload("llama8b"))
         w.update(over)

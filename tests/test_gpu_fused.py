@@ -35,6 +35,8 @@ CASES = {
     "contbatch": dict(lens=[1, 16, 17, 700, 2900], over=dict(batch=5)),
     "gemma_mix": dict(lens=[3001, 5], over=dict(batch=2)),
     "long_mixed": dict(lens=[5000, 777], over=dict(batch=2)),
+    "llama8b_f16": dict(lens=[1000, 33, 2049], over=dict(batch=3)),
+    "long_f16": dict(lens=[3000, 77], over=dict(batch=2)),
 }
 
 
@@ -159,11 +161,12 @@ def _window_step(c: Case, window: int, chunk: int, step: int = 1):
     return q, out.float().cpu().numpy().astype(np.float64), k_new, v_new, pos
 
 
+@pytest.mark.parametrize("name", ["gemma_mix", "llama8b_f16"])
 @pytest.mark.parametrize("chunk", [0, 64])
 @pytest.mark.parametrize("L", [5, 1024, 1153, 3000])
-def test_fused_window_step_matches_oracle(L, chunk):
+def test_fused_window_step_matches_oracle(L, chunk, name):
     """Ring of 1152 rows, window 1024: the new row overwrites ring row (L-1) mod 1152."""
-    w = wl.workload("gemma_mix", batch=1)
+    w = wl.workload(name, batch=1)
     c = Case(w, [L], ring_rows=1152)
     q, got, k_new, v_new, pos = _window_step(c, 1024, chunk)
     assert c.cache.status_bits() == 0

@@ -32,6 +32,8 @@ SMALL = {
     "contbatch": dict(lens=[0, 1, 16, 17, 700, 2900], over=dict(batch=6)),
     "gemma_mix": dict(lens=[3001, 5], over=dict(batch=2)),
     "long_mixed": dict(lens=[5000, 777], over=dict(batch=2)),
+    "llama8b_f16": dict(lens=[1000, 37, 2049], over=dict(batch=3)),
+    "long_f16": dict(lens=[3000, 777], over=dict(batch=2)),
 }
 
 
