@@ -41,6 +41,12 @@ Readings taken where the pages are silent (each also listed in the design doc):
   R8  the unquantised "f16" KV type of [Kaiwu] finding 2 (f16 K + f16 V) stores
       each element of the (rotated, fp32) row rounded once to fp16 (nearest,
       ties to even), with no scale; its value is read back exactly.
+  R9  the "shimmy4" kind is the codec of [Shimmy] §3.2 as written:
+      scale = fl32(max|x| / 7.5) (stored in the param type), code =
+      clamp(round(fl32(x / scale)), -8, 7) with round half away from zero (the
+      Rust ``round`` it uses), nibble = code + 8 (offset binary, even element
+      low), x^ = (nibble - 8) * scale; a zero scale gives code 0.  Groups of
+      any size (the page uses one group per head vector).
 """
 from __future__ import annotations
 
@@ -50,7 +56,7 @@ from dataclasses import dataclass
 import numpy as np
 
 PARAM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
-KV_KINDS = ("sym4", "sym8", "affine4", "f16", "f32")
+KV_KINDS = ("sym4", "sym8", "affine4", "f16", "f32", "shimmy4")
 
 
 # ---------------------------------------------------------------------------
@@ -198,6 +204,24 @@ def quantize_affine(x: np.ndarray, group: int, param: str):
     return c.reshape(*lead, hd), s, b
 
 
+def quantize_shimmy(x: np.ndarray, group: int, param: str):
+    """[Shimmy] §3.2 quantize_head_vector per group (reading R9).
+
+    Returns (codes int8 in [-8, 7], scales fp32).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    lead, hd = x.shape[:-1], x.shape[-1]
+    xg = x.reshape(*lead, hd // group, group)
+    amax = np.max(np.abs(xg), axis=-1)
+    s = round_param((amax / np.float32(7.5)).astype(np.float32), param)
+    safe = np.where(s == 0, np.float32(1.0), s).astype(np.float32)
+    y = (xg / safe[..., None]).astype(np.float32).astype(np.float64)
+    r = np.sign(y) * np.floor(np.abs(y) + 0.5)          # half away from zero, exact in fp64
+    c = np.clip(r, -8, 7)
+    c = np.where((s == 0)[..., None], 0, c).astype(np.int8)
+    return c.reshape(*lead, hd), s
+
+
 def quantize(kind: str, x: np.ndarray, group: int, param: str):
     """(codes, scales, biases-or-None) for any stored kind; "f16" (R8) keeps
     the fp16-rounded values as its codes and has no scales."""
@@ -211,6 +235,9 @@ def quantize(kind: str, x: np.ndarray, group: int, param: str):
         return c, s, None
     if kind == "affine4":
         return quantize_affine(x, group, param)
+    if kind == "shimmy4":
+        c, s = quantize_shimmy(x, group, param)
+        return c, s, None
     raise ValueError(kind)
 
 
@@ -343,6 +370,9 @@ def pack_codes(kind: str, codes: np.ndarray) -> np.ndarray:
         return c.view(np.uint8).reshape(*c.shape[:-1], 2 * c.shape[-1])
     if kind == "sym8":
         return np.asarray(codes, dtype=np.int8).view(np.uint8)
+    if kind == "shimmy4":   # offset-binary nibbles: code + 8
+        c = (np.asarray(codes).astype(np.int16) + 8) & 0xF
+        return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
     c = np.asarray(codes).astype(np.int16) & 0xF
     return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
 
@@ -359,6 +389,9 @@ def unpack_codes(kind: str, raw: np.ndarray) -> np.ndarray:
     if kind == "sym4":
         lo = (lo ^ 8) - 8
         hi = (hi ^ 8) - 8
+    if kind == "shimmy4":
+        lo = lo - 8
+        hi = hi - 8
     out = np.empty(raw.shape[:-1] + (raw.shape[-1] * 2,), dtype=np.int16)
     out[..., 0::2] = lo
     out[..., 1::2] = hi

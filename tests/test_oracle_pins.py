@@ -325,7 +325,8 @@ def _small_spec(**kw):
     return O.Spec(**base)
 
 
-@pytest.mark.parametrize("kinds", [("sym4", "sym4"), ("sym8", "sym4"), ("affine4", "affine4"), ("f16", "f16")])
+@pytest.mark.parametrize("kinds", [("sym4", "sym4"), ("sym8", "sym4"), ("affine4", "affine4"), ("f16", "f16"),
+                                   ("shimmy4", "shimmy4")])
 def test_paged_equals_contiguous(kinds):
     kk, vk = kinds
     par = "bf16" if kk == "affine4" else "f16"
@@ -409,6 +410,37 @@ def test_f16_kv_layout_and_brute_force_attention():
         ref = _brute_attend(q[0, h].tolist(), K16[:, h // 2].tolist(), V16[:, h // 2].tolist(),
                             1.0 / np.sqrt(32.0))
         assert np.allclose(got[0, h], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_shimmy_codec_hand_worked_and_brute_force():
+    """[Shimmy] §3.2 quantize_head_vector (reading R9): scale = max|x| / 7.5,
+    code = clamp(round(x / scale), -8, 7) rounding half away from zero, stored
+    as code + 8 with the even element in the low nibble."""
+    x = np.array([[7.5, -7.5, 2.5, -2.5, 0.5, 3.75, -0.5, 1.25]], np.float32)
+    c, s, b = O.quantize("shimmy4", x, 8, "f32")
+    assert b is None and s[0, 0] == 1.0
+    # 7.5 rounds to 8 and clamps to 7; ties 2.5 / -2.5 / 0.5 / -0.5 go away from zero
+    assert c.tolist() == [[7, -8, 3, -3, 1, 4, -1, 1]]
+    assert O.pack_codes("shimmy4", c).tolist() == [[0x0F, 0x5B, 0xC9, 0x97]]
+    assert O.unpack_codes("shimmy4", O.pack_codes("shimmy4", c)).tolist() == c.tolist()
+    assert O.bytes_per_token_head("shimmy4", 128, 128, "f32") == 68      # 0.53 B per element, as the page says
+    # brute force: the nearest integer in [-8, 7], a tie to the one farther from zero
+    rng = np.random.default_rng(3)
+    xs = rng.standard_normal((64, 32)).astype(np.float32) * rng.uniform(0.1, 5, (64, 1)).astype(np.float32)
+    xs[::7, 5] = 0.0
+    codes, scales, _ = O.quantize("shimmy4", xs, 32, "f32")
+    for r in range(xs.shape[0]):
+        sc = np.float32(np.max(np.abs(xs[r])) / np.float32(7.5))
+        assert scales[r, 0] == sc
+        for j in range(32):
+            y = float(np.float32(xs[r, j] / sc))
+            best = min(range(-8, 8), key=lambda k: (abs(y - k), -abs(k)))
+            assert codes[r, j] == best
+            assert abs(xs[r, j] - codes[r, j] * sc) <= sc / 2 + 1e-6 * sc   # round-trip bound
+    # an all-zero group: scale 0, codes 0 (nibbles 8)
+    z, sz, _ = O.quantize("shimmy4", np.zeros((1, 8), np.float32), 8, "f32")
+    assert sz[0, 0] == 0 and z.tolist() == [[0] * 8]
+    assert O.pack_codes("shimmy4", z).tolist() == [[0x88] * 4]
 
 
 def test_ring_equals_explicit_window():
