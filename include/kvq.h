@@ -93,8 +93,12 @@ typedef enum kvq_kv_dtype {
   KVQ_SYM_INT4 = 0,       /* [airllm] §4.2, [Shimmy] §3.2: symmetric 4-bit */
   KVQ_SYM_INT8 = 1,       /* [Kaiwu] finding 2 "q8_0" K cache: symmetric 8-bit */
   KVQ_AFFINE_INT4 = 2,    /* [Fieldfare] "量化和精度": 4-bit with scale + bias */
-  KVQ_F16_KV = 3,         /* unquantized f16 ([Kaiwu] "f16+f16"); sizing only */
-  KVQ_F32_KV = 4          /* unquantized f32 ([Shimmy] §3.1); sizing only */
+  KVQ_F16_KV = 3,         /* unquantized f16 ([Kaiwu] "f16+f16"): fp16 rows, no scale;
+                             decode with head_dim 64 or 128 */
+  KVQ_F32_KV = 4,         /* unquantized f32 ([Shimmy] §3.1); sizing only */
+  KVQ_SHIMMY_INT4 = 5     /* [Shimmy] §3.2 as written: scale = max|x| / 7.5,
+                             code = clamp(round(x / scale), -8, 7) rounding half away
+                             from zero, stored as code + 8; f32 scales */
 } kvq_kv_dtype;
 
 typedef enum kvq_rope {

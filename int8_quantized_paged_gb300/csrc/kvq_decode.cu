@@ -97,6 +97,7 @@ static int max_active_clusters(TcLaunch fn, const TcArgs& t, int hd, int nt, int
 // The tensor-core launcher of a config's K/V kinds and scale type.
 static TcLaunch tc_launcher(const kvq_config& c) {
   if (c.k_dtype == KVQ_F16_KV) return launch_tc_h16;   // no scales: one instantiation
+  if (c.k_dtype == KVQ_SHIMMY_INT4) return launch_tc_o4o4_f32;   // f32 scales only
   static const TcLaunch table[4][3] = {
       {launch_tc_s4s4_f32, launch_tc_s4s4_f16, launch_tc_s4s4_bf16},
       {launch_tc_s8s8_f32, launch_tc_s8s8_f16, launch_tc_s8s8_bf16},
@@ -371,8 +372,9 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     return fn(t, hd, nt, ng, lc);
   }
 
-  if (k == KVQ_F16_KV)
-    return fail(KVQ_ERR_UNSUPPORTED, "f16 K/V: no tensor-core kernel for head_dim %d and G %d", cfg->head_dim, G);
+  if (k == KVQ_F16_KV || k == KVQ_SHIMMY_INT4)
+    return fail(KVQ_ERR_UNSUPPORTED, "K/V kind %d: only the tensor-core kernel, which does not take head_dim %d, G %d",
+                k, cfg->head_dim, G);
   const dim3 grid(w.n_chunks, cfg->n_kv_heads, batch);
   kvq_status st;
   if (k == KVQ_SYM_INT4 && v == KVQ_SYM_INT4) st = launch_decode_s4s4(a, cfg->head_dim, G, grid, stream);

@@ -242,6 +242,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   constexpr int D = tc_depth(HD, NT, KK);       // pages in flight per warp
   constexpr bool K8 = KK == KVQ_SYM_INT8, V8 = VK == KVQ_SYM_INT8;
   constexpr bool KAFF = KK == KVQ_AFFINE_INT4, VAFF = VK == KVQ_AFFINE_INT4;
+  // 4-bit conversion modes (kvq_tc_ptx.cuh): 0 symmetric, 1 affine, 2 offset-binary (shimmy4)
+  constexpr int KQ4 = KAFF ? 1 : (KK == KVQ_SHIMMY_INT4 ? 2 : 0);
+  constexpr int VQ4 = VAFF ? 1 : (VK == KVQ_SHIMMY_INT4 ? 2 : 0);
   // F16: unquantised fp16 K and V (no scales): the ldmatrix fragments are the
   // MMA operands as they are, and the stored scales below read as 1
   constexpr bool F16 = KK == KVQ_F16_KV;
@@ -789,10 +792,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         } else {              // k-steps 2c, 2c+1: the uint4 of chunk c
           const uint32_t be0[2] = {qf[0][cc][0], qf[0][cc][1]}, bo0[2] = {qf[0][cc][2], qf[0][cc][3]};
           if constexpr (NT == 1) {
-            tc::qk4<KAFF>(r[2 * cc], r[2 * cc + 1], be0, bo0, sacc[0]);
+            tc::qk4<KQ4>(r[2 * cc], r[2 * cc + 1], be0, bo0, sacc[0]);
           } else {
             const uint32_t be1[2] = {qf[1][cc][0], qf[1][cc][1]}, bo1[2] = {qf[1][cc][2], qf[1][cc][3]};
-            tc::qk4x2<KAFF>(r[2 * cc], r[2 * cc + 1], be0, bo0, be1, bo1, sacc[0], sacc[1]);
+            tc::qk4x2<KQ4>(r[2 * cc], r[2 * cc + 1], be0, bo0, be1, bo1, sacc[0], sacc[1]);
           }
         }
         if constexpr (!ONEG) {
@@ -959,9 +962,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
           for (int nt = 0; nt < NT; ++nt) tc::pv8(y[2 * cc], y[2 * cc + 1], bw[nt], oacc[c][MRG ? 0 : nt]);
         } else {
           if constexpr (NT == 1)
-            tc::pv4<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], oacc[2 * c][0], oacc[2 * c + 1][0]);
+            tc::pv4<VQ4>(y[2 * cc], y[2 * cc + 1], bw[0], oacc[2 * c][0], oacc[2 * c + 1][0]);
           else
-            tc::pv4m<VAFF>(y[2 * cc], y[2 * cc + 1], bw[0], bw[1], oacc[2 * c][0], oacc[2 * c + 1][0]);
+            tc::pv4m<VQ4>(y[2 * cc], y[2 * cc + 1], bw[0], bw[1], oacc[2 * c][0], oacc[2 * c + 1][0]);
         }
       }
     }
@@ -1424,6 +1427,7 @@ KVQ_TC_DECLARE(launch_tc_a4a4_f32)
 KVQ_TC_DECLARE(launch_tc_a4a4_f16)
 KVQ_TC_DECLARE(launch_tc_a4a4_bf16)
 KVQ_TC_DECLARE(launch_tc_h16)
+KVQ_TC_DECLARE(launch_tc_o4o4_f32)
 #undef KVQ_TC_DECLARE
 
 }  // namespace kvq

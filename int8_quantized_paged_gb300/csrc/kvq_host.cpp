@@ -50,7 +50,7 @@ static kvq_status check_common(const kvq_config* c) {
   const int32_t params[2] = {c->k_param_dtype, c->v_param_dtype};
   for (int i = 0; i < 2; ++i) {
     const char* kv = i ? "v" : "k";
-    if (kinds[i] < KVQ_SYM_INT4 || kinds[i] > KVQ_F32_KV)
+    if (kinds[i] < KVQ_SYM_INT4 || kinds[i] > KVQ_SHIMMY_INT4)
       return fail(KVQ_ERR_INVALID_ARG, "%s_dtype %d is not a kvq_kv_dtype", kv, kinds[i]);
     if (!is_quant_kind(kinds[i])) continue;
     if (groups[i] < 2 || c->head_dim % groups[i] != 0 || groups[i] % 2 != 0)
@@ -83,11 +83,17 @@ kvq_status check_kernel_config(const kvq_config* c) {
                        (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT8) ||
                        (k == KVQ_SYM_INT8 && v == KVQ_SYM_INT4) ||
                        (k == KVQ_AFFINE_INT4 && v == KVQ_AFFINE_INT4) ||
-                       (k == KVQ_F16_KV && v == KVQ_F16_KV);
+                       (k == KVQ_F16_KV && v == KVQ_F16_KV) ||
+                       (k == KVQ_SHIMMY_INT4 && v == KVQ_SHIMMY_INT4);
   if (!pair_ok)
     return fail(KVQ_ERR_UNSUPPORTED,
                 "K/V dtype pair (%d, %d); kernels exist for sym4/sym4, sym8/sym8, sym8/sym4, "
-                "affine4/affine4, f16/f16", k, v);
+                "affine4/affine4, f16/f16, shimmy4/shimmy4", k, v);
+  if (k == KVQ_SHIMMY_INT4) {   // the tensor-core kernel only: f32 scales, groups of 2^n >= 32
+    if (c->k_param_dtype != KVQ_F32 || c->v_param_dtype != KVQ_F32 || c->k_group != c->v_group ||
+        c->k_group < 32 || (c->k_group & (c->k_group - 1)) != 0)
+      return fail(KVQ_ERR_UNSUPPORTED, "shimmy4 K/V: kernels exist for f32 scales and equal power-of-two groups >= 32");
+  }
   if (k == KVQ_F16_KV) {   // unquantised: no groups; the tensor-core kernel only
     if (c->head_dim == 256)
       return fail(KVQ_ERR_UNSUPPORTED, "f16 K/V: kernels exist for head_dim 64 and 128");

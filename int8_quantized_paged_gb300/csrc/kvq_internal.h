@@ -22,7 +22,7 @@ kvq_status fail(kvq_status st, const char* fmt, ...);
 // Stored parameter type (same numbering as kvq_float).
 KVQ_HD inline int param_bytes(int f) { return f == KVQ_F32 ? 4 : 2; }
 KVQ_HD inline bool is_quant_kind(int k) {
-  return k == KVQ_SYM_INT4 || k == KVQ_SYM_INT8 || k == KVQ_AFFINE_INT4;
+  return k == KVQ_SYM_INT4 || k == KVQ_SYM_INT8 || k == KVQ_AFFINE_INT4 || k == KVQ_SHIMMY_INT4;
 }
 
 // Byte layout of one pool (see the storage format in kvq.h).

@@ -57,6 +57,14 @@ __device__ __forceinline__ float rint_quotient(float x, float s, float r) {
   if (fabsf(t - 0.5f) > 6.103515625e-05f) return rintf(y);
   return rintf(__fdiv_rn(x, s));
 }
+// The same with round half away from zero (roundf): its boundaries are the
+// same half-integers.
+__device__ __forceinline__ float round_quotient(float x, float s, float r) {
+  const float y = __fmul_rn(x, r);
+  const float t = y - floorf(y);
+  if (fabsf(t - 0.5f) > 6.103515625e-05f) return roundf(y);
+  return roundf(__fdiv_rn(x, s));
+}
 
 // The lane's quantized row piece: its packed code bytes (DPL/2 for 4-bit
 // kinds, DPL for 8-bit, little-endian in w) and its group's parameters.
@@ -107,6 +115,22 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
     }
     r.scale = scale;
     r.bias = bias;
+  } else if (L.kind == KVQ_SHIMMY_INT4) {
+    // [Shimmy] §3.2: scale = max|x| / 7.5, code = clamp(round(x / scale), -8, 7)
+    // (half away from zero), stored as code + 8; a zero scale gives code 0
+    float amax = fabsf(x[0]);
+#pragma unroll
+    for (int j = 1; j < DPL; ++j) amax = fmaxf(amax, fabsf(x[j]));
+    for (int o = 1; o < lpg; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = round_param(__fdiv_rn(amax, 7.5f), L.param);
+    const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) {
+      float y = scale == 0.0f ? 0.0f : round_quotient(x[j], scale, rs);
+      y = fminf(fmaxf(y, -8.0f), 7.0f);
+      c[j] = (int)y + 8;
+    }
+    r.scale = scale;
   } else {
     const float qmax = L.kind == KVQ_SYM_INT8 ? 127.0f : 7.0f;
     float amax = fabsf(x[0]);

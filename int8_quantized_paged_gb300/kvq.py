@@ -21,11 +21,12 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OUT_OF_PAGES, ERR_BAD_BLOCK_TABLE, \
     ERR_WORKSPACE_TOO_SMALL, ERR_CUDA = range(7)
 DEV_BAD_PAGE, DEV_BAD_POS, DEV_BAD_SEQ, DEV_BAD_LEN = 1, 2, 4, 8
 F32, F16, BF16 = 0, 1, 2
-SYM_INT4, SYM_INT8, AFFINE_INT4, F16_KV, F32_KV = range(5)
+SYM_INT4, SYM_INT8, AFFINE_INT4, F16_KV, F32_KV, SHIMMY_INT4 = range(6)
 ROPE_NONE, ROPE_NORMAL, ROPE_NEOX = 0, 1, 2
 
 FLOATS = {"f32": F32, "f16": F16, "bf16": BF16}
-KINDS = {"sym4": SYM_INT4, "sym8": SYM_INT8, "affine4": AFFINE_INT4, "f16": F16_KV, "f32": F32_KV}
+KINDS = {"sym4": SYM_INT4, "sym8": SYM_INT8, "affine4": AFFINE_INT4, "f16": F16_KV, "f32": F32_KV,
+         "shimmy4": SHIMMY_INT4}
 ROPES = {"none": ROPE_NONE, "normal": ROPE_NORMAL, "neox": ROPE_NEOX}
 
 

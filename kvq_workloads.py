@@ -29,6 +29,8 @@ from a seeded numpy ``Generator``):
 * ``llama8b_f16``, ``long_f16`` -- the ``llama8b`` and ``long_mixed`` shapes
                   with unquantised f16 K and V (the "f16+f16" KV type the
                   pages compare the quantised ones with).
+* ``llama8b_shimmy`` -- the ``llama8b`` shape with the /7.5 offset-8 4-bit
+                  codec of the Shimmy post ("shimmy4").
 """
 from __future__ import annotations
 
@@ -36,7 +38,7 @@ import numpy as np
 
 # Plain descriptions of each workload.  Strings name the codec kinds:
 #   "sym4"  symmetric 4-bit, "sym8" symmetric 8-bit, "affine4" affine 4-bit,
-#   "f16"   unquantised f16.
+#   "f16"   unquantised f16, "shimmy4" the /7.5 offset-8 4-bit codec.
 WORKLOADS: dict[str, dict] = {
     "tiny": dict(
         index=0, batch=1, n_heads=4, n_kv_heads=2, head_dim=64, ctx=256,
@@ -71,6 +73,7 @@ WORKLOADS: dict[str, dict] = {
 }
 
 WORKLOADS["llama8b_f16"] = dict(WORKLOADS["llama8b"], index=5, k_kind="f16", v_kind="f16")
+WORKLOADS["llama8b_shimmy"] = dict(WORKLOADS["llama8b"], index=7, k_kind="shimmy4", v_kind="shimmy4")
 WORKLOADS["long_f16"] = dict(WORKLOADS["long_mixed"], index=6, k_kind="f16", v_kind="f16", k_group=128,
                              v_group=128, k_param="f32", v_param="f32")
 

@@ -109,9 +109,12 @@ def test_validate_config():
         (dict(k_kind="sym4", v_kind="sym8"), kvq.ERR_UNSUPPORTED),
         (dict(k_kind="f16", v_kind="f16", head_dim=256, k_group=256, v_group=256), kvq.ERR_UNSUPPORTED),
         (dict(k_kind="f16", v_kind="sym4"), kvq.ERR_UNSUPPORTED),
+        (dict(k_kind="shimmy4", v_kind="shimmy4", k_param="f16", v_param="f16"), kvq.ERR_UNSUPPORTED),
+        (dict(k_kind="shimmy4", v_kind="shimmy4", k_group=16, v_group=16), kvq.ERR_UNSUPPORTED),
         (dict(rope_base=-1.0), kvq.ERR_INVALID_ARG),
     ]
     kvq.validate_config(_cfg(wl.workload("llama8b_f16")))   # unquantised f16 K/V at head_dim 128
+    kvq.validate_config(_cfg(wl.workload("llama8b_shimmy")))  # the /7.5 offset-8 codec
     for over, want in bad:
         w = dict(wl.workload("llama8b"))
         w.update(over)

@@ -34,6 +34,7 @@ SMALL = {
     "long_mixed": dict(lens=[5000, 777], over=dict(batch=2)),
     "llama8b_f16": dict(lens=[1000, 37, 2049], over=dict(batch=3)),
     "long_f16": dict(lens=[3000, 777], over=dict(batch=2)),
+    "llama8b_shimmy": dict(lens=[1000, 37, 2049], over=dict(batch=3)),
 }
 
 
@@ -223,7 +224,7 @@ def _tie_rows(w: dict, n_rows: int, seed: int) -> np.ndarray:
     (k + 1/2) * scale for the scale the quantizer will store."""
     rng = np.random.default_rng(seed)
     hkv, hd, g = w["n_kv_heads"], w["head_dim"], w["k_group"]
-    qmax = 127.0 if w["k_kind"] == "sym8" else 7.0
+    qmax = {"sym8": 127.0, "shimmy4": 7.5}.get(w["k_kind"], 7.0)
     rows = np.zeros((n_rows, hkv, hd), np.float32)
     for r in range(n_rows):
         for h in range(hkv):
@@ -233,7 +234,7 @@ def _tie_rows(w: dict, n_rows: int, seed: int) -> np.ndarray:
                 scale = np.float32(np.float32(amax) / np.float32(qmax))
                 if w["k_param"] == "f16":
                     scale = np.float32(np.float16(scale))
-                ks = rng.integers(-int(qmax), int(qmax), g).astype(np.float32) + np.float32(0.5)
+                ks = rng.integers(-int(qmax + 0.5), int(qmax), g).astype(np.float32) + np.float32(0.5)
                 x = (ks * scale).astype(np.float32)
                 nudge = rng.integers(-2, 3, g)
                 x = np.array([np.nextafter(v, np.float32(np.inf) if d > 0 else np.float32(-np.inf))
@@ -246,6 +247,7 @@ def _tie_rows(w: dict, n_rows: int, seed: int) -> np.ndarray:
 @pytest.mark.parametrize("name,over", [
     ("tiny", dict(rope="none")),
     ("long_mixed", dict(rope="none", act="f32", k_kind="sym8", v_kind="sym8")),
+    ("llama8b", dict(rope="none", act="f32", k_kind="shimmy4", v_kind="shimmy4")),
 ])
 def test_append_codes_at_rounding_ties(name, over):
     """Codes of quotients at and next to rounding ties: the append kernel and
