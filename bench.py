@@ -48,6 +48,9 @@ MODELS = {
     # the unquantised f16 K/V the pages compare with (8K and 64K)
     "llama8b_f16": [("llama8b_f16", 32, False)],
     "long_f16": [("long_f16", 4, False)],
+    # the /7.5 offset-8 4-bit codec (8K and 64K)
+    "llama8b_shimmy": [("llama8b_shimmy", 32, False)],
+    "long_shimmy": [("long_shimmy", 4, False)],
 }
 
 

@@ -43,15 +43,21 @@
  * page_size], slot r % page_size ([airllm] §2.3: fixed-size blocks from a free
  * pool, an offset index inside each block).
  *
- * Codec (readings listed in the design doc).  All of it is IEEE fp32 with one
- * rounding per operation and no fused multiply-add.  Rounding is to nearest,
- * ties to even.  The resulting codes are bit-exact across implementations.
+ * Codec.  All of it is IEEE fp32 with one rounding per operation and no
+ * fused multiply-add.  Rounding is to nearest, ties to even, except where a
+ * kind says otherwise.  The resulting codes are bit-exact across
+ * implementations.
  *   symmetric ([airllm] §4.2 group_quantize; [Shimmy] §3.2):
  *     s  = stored(max(amax / Qmax, floor)),  Qmax = 7 (4-bit) or 127 (8-bit),
  *     floor = 2^-14 for f16 scales, else 1e-8;  code = clamp(rne(x / s), +-Qmax)
  *   affine ([Fieldfare] "量化和精度": 4-bit, group 64, bf16 scale + bias):
  *     s = stored((max - min) / 15),  b = stored(min),
  *     code = s == 0 ? 0 : clamp(rne((x - b) / s), 0, 15);   x^ = s*code + b
+ *   offset-8 4-bit ([Shimmy] §3.2 quantize_head_vector; KVQ_SHIMMY_INT4):
+ *     s = stored(amax / 7.5),  code = s == 0 ? 0 : clamp(round(x / s), -8, 7)
+ *     with round half away from zero, nibble = code + 8;  x^ = (nibble - 8)*s
+ *   f16 ([Kaiwu] finding 2, "f16+f16"; KVQ_F16_KV): each element rounded
+ *     once to fp16, no scale.
  *   K is rotated (RoPE, fp32) at its own position before it is quantized; V
  *   is not ([Fieldfare] "KV Cache 的双布局设计").
  */

@@ -29,8 +29,9 @@ from a seeded numpy ``Generator``):
 * ``llama8b_f16``, ``long_f16`` -- the ``llama8b`` and ``long_mixed`` shapes
                   with unquantised f16 K and V (the "f16+f16" KV type the
                   pages compare the quantised ones with).
-* ``llama8b_shimmy`` -- the ``llama8b`` shape with the /7.5 offset-8 4-bit
-                  codec of the Shimmy post ("shimmy4").
+* ``llama8b_shimmy``, ``long_shimmy`` -- the ``llama8b`` and ``long_mixed``
+                  shapes with the /7.5 offset-8 4-bit codec of the Shimmy post
+                  ("shimmy4"), one fp32 scale per 128-element head vector.
 """
 from __future__ import annotations
 
@@ -76,6 +77,8 @@ WORKLOADS["llama8b_f16"] = dict(WORKLOADS["llama8b"], index=5, k_kind="f16", v_k
 WORKLOADS["llama8b_shimmy"] = dict(WORKLOADS["llama8b"], index=7, k_kind="shimmy4", v_kind="shimmy4")
 WORKLOADS["long_f16"] = dict(WORKLOADS["long_mixed"], index=6, k_kind="f16", v_kind="f16", k_group=128,
                              v_group=128, k_param="f32", v_param="f32")
+WORKLOADS["long_shimmy"] = dict(WORKLOADS["long_mixed"], index=8, k_kind="shimmy4", v_kind="shimmy4",
+                                k_group=128, v_group=128, k_param="f32", v_param="f32")
 
 ACT_NUMPY = {"f32": np.float32, "f16": np.float16}
 

@@ -21,9 +21,11 @@ the numeric spec fixes it, because a quantised code is an integer decided by
 floating point and both sides must decide it in the same precision.  Everything
 after the codes (dequantisation, q rotation, scores, softmax, P.V) is fp64.
 
-Readings taken where the pages are silent (each also listed in the design doc):
-  R1  round-half-to-even for x/scale (torch.round in [airllm] §4.2 rounds half
-      to even; the Rust ``round()`` of [Shimmy] §3.2 does not and is not used).
+Readings taken where the pages are silent:
+  R1  round-half-to-even for x/scale in the symmetric and affine kinds
+      (torch.round in [airllm] §4.2 rounds half to even); the Rust ``round()``
+      of [Shimmy] §3.2 rounds half away from zero and serves only its own
+      codec, the "shimmy4" kind (R9).
   R2  symmetric scale = max|x| / 7 with clamp_min 1e-8 ([airllm] §4.2); for
       fp16-stored scales the floor is 2^-14 (1e-8 underflows in fp16); the
       floor is applied in fp32 before rounding to the stored type.

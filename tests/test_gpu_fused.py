@@ -38,6 +38,7 @@ CASES = {
     "llama8b_f16": dict(lens=[1000, 33, 2049], over=dict(batch=3)),
     "long_f16": dict(lens=[3000, 77], over=dict(batch=2)),
     "llama8b_shimmy": dict(lens=[1000, 33, 2049], over=dict(batch=3)),
+    "long_shimmy": dict(lens=[3000, 77], over=dict(batch=2)),
 }
 
 

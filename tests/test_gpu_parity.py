@@ -35,6 +35,7 @@ SMALL = {
     "llama8b_f16": dict(lens=[1000, 37, 2049], over=dict(batch=3)),
     "long_f16": dict(lens=[3000, 777], over=dict(batch=2)),
     "llama8b_shimmy": dict(lens=[1000, 37, 2049], over=dict(batch=3)),
+    "long_shimmy": dict(lens=[3000, 777], over=dict(batch=2)),
 }
 
 
