@@ -209,6 +209,33 @@ def test_wide_query_groups_match_oracle(heads, chunk):
     assert c.cache.status_bits() == 0
 
 
+@pytest.mark.parametrize("chunk", [0, 64])
+@pytest.mark.parametrize("heads", [(8, 8), (16, 8), (32, 8), (64, 8)])
+@pytest.mark.parametrize("kv", [("sym8", "sym4", 32, "f16"), ("sym4", "sym4", 64, "f32"),
+                                ("sym8", "sym8", 32, "bf16")])
+def test_several_v_groups_match_oracle(kv, heads, chunk):
+    """Symmetric V with several groups per head vector at G = 1, 2, 4 and 8:
+    the weights of each group are formed in the P.V operand layout.  1 % of
+    the elements x 8 move the groups' reference scales up between pages."""
+    kk, vk, g, par = kv
+    w = wl.workload("long_mixed", batch=2, n_heads=heads[0], n_kv_heads=heads[1], k_kind=kk, v_kind=vk,
+                    k_group=g, v_group=g, k_param=par, v_param=par)
+    c = Case(w, [1500, 41])
+    q = c.queries()
+    assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q)) <= TOL
+    assert c.cache.status_bits() == 0
+
+
+def test_several_v_groups_window_matches_oracle():
+    """The same weights at the window's first page, which starts mid-page."""
+    w = wl.workload("long_mixed", batch=2, n_heads=32, n_kv_heads=4, ctx=4096)
+    c = Case(w, [1500, 3000], ring_rows=1152)
+    q = c.queries()
+    ref = c.oracle_decode(q, window=1000)
+    for chunk in (0, 64):
+        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk, window=1000), ref) <= TOL
+
+
 def test_wide_query_group_affine_matches_oracle():
     """G = 8 with affine 4-bit K/V (per-group q sums of the 8 heads)."""
     w = wl.workload("gemma_mix", batch=2, n_heads=64, n_kv_heads=8, head_dim=128)
