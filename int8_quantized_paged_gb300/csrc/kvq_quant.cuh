@@ -77,14 +77,17 @@ struct RowCodes {
   bool leader;    // the first lane of its group: writes the parameters
 };
 
-template <int DPL>
+// KIND: the row's kind when the caller knows it at compile time (the decode
+// kernel: only that kind's code is compiled in), else -1 for L.kind.
+template <int DPL, int KIND = -1>
 __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const PoolLayout& L, int lane) {
+  const int kind = KIND >= 0 ? KIND : L.kind;
   const int lpg = L.group / DPL;   // lanes per group (a power of two)
   RowCodes r;
   r.group = lane / lpg;
   r.leader = lane % lpg == 0;
   r.bias = 0.f;
-  if (L.kind == KVQ_F16_KV) {   // unquantised: the fp16 rounding of each element, no parameters
+  if (kind == KVQ_F16_KV) {   // unquantised: the fp16 rounding of each element, no parameters
     uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int j = 0; j < DPL; ++j)
@@ -96,7 +99,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
     return r;
   }
   int c[DPL];
-  if (L.kind == KVQ_AFFINE_INT4) {
+  if (kind == KVQ_AFFINE_INT4) {
     float mn = x[0], mx = x[0];
 #pragma unroll
     for (int j = 1; j < DPL; ++j) { mn = fminf(mn, x[j]); mx = fmaxf(mx, x[j]); }
@@ -115,7 +118,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
     }
     r.scale = scale;
     r.bias = bias;
-  } else if (L.kind == KVQ_SHIMMY_INT4) {
+  } else if (kind == KVQ_SHIMMY_INT4) {
     // [Shimmy] §3.2: scale = max|x| / 7.5, code = clamp(round(x / scale), -8, 7)
     // (half away from zero), stored as code + 8; a zero scale gives code 0
     float amax = fabsf(x[0]);
@@ -132,7 +135,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
     }
     r.scale = scale;
   } else {
-    const float qmax = L.kind == KVQ_SYM_INT8 ? 127.0f : 7.0f;
+    const float qmax = kind == KVQ_SYM_INT8 ? 127.0f : 7.0f;
     float amax = fabsf(x[0]);
 #pragma unroll
     for (int j = 1; j < DPL; ++j) amax = fmaxf(amax, fabsf(x[j]));
@@ -149,7 +152,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
     r.scale = scale;
   }
   uint32_t w[2] = {0u, 0u};
-  if (L.kind == KVQ_SYM_INT8) {
+  if (kind == KVQ_SYM_INT8) {
 #pragma unroll
     for (int j = 0; j < DPL; ++j) w[j / 4] |= ((uint32_t)c[j] & 0xFFu) << (8 * (j % 4));
     r.nbytes = DPL;
