@@ -359,6 +359,34 @@ def build_layers(args, dev, seed: int) -> list:
     return layers
 
 
+def stage_io(layers, dev):
+    """Every layer's step inputs (q, k_new, v_new) as views of one device buffer
+    and its outputs as views of another: a step's inputs then come over from
+    host memory in one copy and its outputs go back in one, as a server would
+    batch them.  Each view starts on a multiple of head_dim elements (>= 128 B).
+    Returns (inputs, outputs), the two flat buffers."""
+    import torch
+    act = layers[0].q.dtype
+    assert all(L.q.dtype == act for L in layers), "one activation dtype per model"
+
+    def pack(tensors):
+        buf = torch.empty(sum(t.numel() for t in tensors), dtype=act, device=dev)
+        views, o = [], 0
+        for t in tensors:
+            v = buf[o:o + t.numel()].view(t.shape)
+            v.copy_(t)
+            views.append(v)
+            o += t.numel()
+        return buf, views
+
+    io_in, v_in = pack([t for L in layers for t in (L.q, L.k_new, L.v_new)])
+    io_out, v_out = pack([L.out for L in layers])
+    for i, L in enumerate(layers):
+        L.q, L.k_new, L.v_new = v_in[3 * i:3 * i + 3]
+        L.out = v_out[i]
+    return io_in, io_out
+
+
 def run_profile(args) -> None:
     """The timed decode call of every layer (the fused append + decode call, or the
     decode alone), layer after layer, for profiler captures (no timing)."""
@@ -390,6 +418,7 @@ def run_gpu(args) -> dict | None:
     from int8_quantized_paged_gb300 import kvq
 
     layers = build_layers(args, dev, 1000 + 97 * rank)
+    io_in, io_out = stage_io(layers, dev)
     torch.cuda.synchronize()
     for L in layers:
         assert L.cache.status_bits() == 0, "prefill flagged a bad page or position"
@@ -456,24 +485,21 @@ def run_gpu(args) -> dict | None:
             dec_ms.extend(cu.elapsed_ms(e0, e1) for e0, e1 in evs)
     torch.cuda.synchronize()
 
-    # end to end: pinned host inputs -> device, the step, outputs -> pinned host
-    h_in = [[t.cpu().pin_memory() for t in (L.q, L.k_new, L.v_new)] for L in layers]
-    h_out = [L.out.cpu().pin_memory() for L in layers]
-    h2d = sum(t.numel() * t.element_size() for ts in h_in for t in ts)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    # end to end: every layer's inputs from pinned host memory in one copy, the
+    # step (the public call per layer), every layer's outputs back in one copy
+    h_in = io_in.cpu().pin_memory()
+    h_out = io_out.cpu().pin_memory()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(args.steps):
-            for L, (hq, hk, hv) in zip(layers, h_in):
-                L.q.copy_(hq, non_blocking=True)
-                L.k_new.copy_(hk, non_blocking=True)
-                L.v_new.copy_(hv, non_blocking=True)
+            io_in.copy_(h_in, non_blocking=True)
             g_a.replay()
-            for L, ho in zip(layers, h_out):
-                ho.copy_(L.out, non_blocking=True)
+            h_out.copy_(io_out, non_blocking=True)
             stream.synchronize()
         e1.record(stream)
     torch.cuda.synchronize()
