@@ -106,7 +106,7 @@ __host__ __device__ constexpr int tc_pre_bytes(int hd, int nt, int ng) {
 
 // Fused append: quantizes the staged row (K rotated at its position) exactly
 // as the append kernel does.
-template <int HD, int KIND>
+template <int HD, int KIND, int PT>
 __device__ __forceinline__ RowCodes tc_append_row(const uint8_t* row, int act, const float2* cs, int rope,
                                                   const PoolLayout& L, int lane) {
   constexpr int DPL = HD / 32;
@@ -114,7 +114,7 @@ __device__ __forceinline__ RowCodes tc_append_row(const uint8_t* row, int act, c
 #pragma unroll
   for (int j = 0; j < DPL; ++j) x[j] = load_act(row, act, lane * DPL + j);
   if (cs) rope_rotate_row<DPL>(x, cs, rope, lane);
-  return quantize_row<DPL, KIND>(x, L, lane);
+  return quantize_row<DPL, KIND, PT>(x, L, lane);
 }
 
 // Shared-memory offset of 16-byte chunk `c` of row `r` in a block of rows of
@@ -457,24 +457,24 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     const int r = apos % P;
     if (app_role == 1) {
       const float2* cs = a.rope != KVQ_ROPE_NONE ? reinterpret_cast<const float2*>(st + 8 * HD) : nullptr;
-      const RowCodes kq = tc_append_row<HD, KK>(st, a.act, cs, a.rope, a.kl, lane);
-      store_row(kq, a.kl,
+      const RowCodes kq = tc_append_row<HD, KK, PT>(st, a.act, cs, a.rope, a.kl, lane);
+      store_row<KK, PT>(kq, a.kl,
                 const_cast<uint8_t*>(a.k_pool) + (int64_t)app_pg * a.kl.page_bytes + (int64_t)kvh * a.kl.sub_bytes,
                 r, lane);
       store_code_bytes(smem + qk_off + lane * kq.nbytes, kq.w, kq.nbytes);
       if (kq.leader) {
-        store_param(smem + qkp_off + param_scale_offset(a.kl, kq.group), a.kl.param, kq.scale);
-        if (KAFF) store_param(smem + qkp_off + param_bias_offset(a.kl, kq.group), a.kl.param, kq.bias);
+        store_param(smem + qkp_off + param_scale_offset<KK, PT>(a.kl, kq.group), PT, kq.scale);
+        if (KAFF) store_param(smem + qkp_off + param_bias_offset<PT>(a.kl, kq.group), PT, kq.bias);
       }
     } else {
-      const RowCodes vq = tc_append_row<HD, VK>(st + 4 * HD, a.act, nullptr, a.rope, a.vl, lane);
-      store_row(vq, a.vl,
+      const RowCodes vq = tc_append_row<HD, VK, PT>(st + 4 * HD, a.act, nullptr, a.rope, a.vl, lane);
+      store_row<VK, PT>(vq, a.vl,
                 const_cast<uint8_t*>(a.v_pool) + (int64_t)app_pg * a.vl.page_bytes + (int64_t)kvh * a.vl.sub_bytes,
                 r, lane);
       store_code_bytes(smem + qv_off + lane * vq.nbytes, vq.w, vq.nbytes);
       if (vq.leader) {
-        store_param(smem + qvp_off + param_scale_offset(a.vl, vq.group), a.vl.param, vq.scale);
-        if (VAFF) store_param(smem + qvp_off + param_bias_offset(a.vl, vq.group), a.vl.param, vq.bias);
+        store_param(smem + qvp_off + param_scale_offset<VK, PT>(a.vl, vq.group), PT, vq.scale);
+        if (VAFF) store_param(smem + qvp_off + param_bias_offset<PT>(a.vl, vq.group), PT, vq.bias);
       }
     }
   };

@@ -77,11 +77,13 @@ struct RowCodes {
   bool leader;    // the first lane of its group: writes the parameters
 };
 
-// KIND: the row's kind when the caller knows it at compile time (the decode
-// kernel: only that kind's code is compiled in), else -1 for L.kind.
-template <int DPL, int KIND = -1>
+// KIND, PT: the row's kind and parameter type when the caller knows them at
+// compile time (the decode kernel: only that kind's code is compiled in),
+// else -1 for L.kind and L.param.
+template <int DPL, int KIND = -1, int PT = -1>
 __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const PoolLayout& L, int lane) {
   const int kind = KIND >= 0 ? KIND : L.kind;
+  const int param = PT >= 0 ? PT : L.param;
   const int lpg = L.group / DPL;   // lanes per group (a power of two)
   RowCodes r;
   r.group = lane / lpg;
@@ -107,8 +109,8 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
-    const float scale = round_param(__fdiv_rn(__fsub_rn(mx, mn), 15.0f), L.param);
-    const float bias = round_param(mn, L.param);
+    const float scale = round_param(__fdiv_rn(__fsub_rn(mx, mn), 15.0f), param);
+    const float bias = round_param(mn, param);
     const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
 #pragma unroll
     for (int j = 0; j < DPL; ++j) {
@@ -125,7 +127,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
 #pragma unroll
     for (int j = 1; j < DPL; ++j) amax = fmaxf(amax, fabsf(x[j]));
     for (int o = 1; o < lpg; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = round_param(__fdiv_rn(amax, 7.5f), L.param);
+    const float scale = round_param(__fdiv_rn(amax, 7.5f), param);
     const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
 #pragma unroll
     for (int j = 0; j < DPL; ++j) {
@@ -140,8 +142,8 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
 #pragma unroll
     for (int j = 1; j < DPL; ++j) amax = fmaxf(amax, fabsf(x[j]));
     for (int o = 1; o < lpg; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float floor_s = L.param == KVQ_F16 ? 6.103515625e-05f : 1e-8f;
-    const float scale = round_param(fmaxf(__fdiv_rn(amax, qmax), floor_s), L.param);
+    const float floor_s = param == KVQ_F16 ? 6.103515625e-05f : 1e-8f;
+    const float scale = round_param(fmaxf(__fdiv_rn(amax, qmax), floor_s), param);
     const float rs = __frcp_rn(scale);
 #pragma unroll
     for (int j = 0; j < DPL; ++j) {
@@ -165,12 +167,16 @@ __device__ __forceinline__ RowCodes quantize_row(const float (&x)[DPL], const Po
   return r;
 }
 
-// Byte offsets of a group's scale and (affine) bias inside a parameter row.
+// Byte offsets of a group's scale and (affine) bias inside a parameter row
+// (KIND, PT as for quantize_row).
+template <int KIND = -1, int PT = -1>
 __device__ __forceinline__ int param_scale_offset(const PoolLayout& L, int g) {
-  return (L.kind == KVQ_AFFINE_INT4 ? 2 * g : g) * param_bytes(L.param);
+  const int kind = KIND >= 0 ? KIND : L.kind;
+  return (kind == KVQ_AFFINE_INT4 ? 2 * g : g) * param_bytes(PT >= 0 ? PT : L.param);
 }
+template <int PT = -1>
 __device__ __forceinline__ int param_bias_offset(const PoolLayout& L, int g) {
-  return (2 * g + 1) * param_bytes(L.param);
+  return (2 * g + 1) * param_bytes(PT >= 0 ? PT : L.param);
 }
 
 // Writes `nbytes` (1, 2, 4, 8 or 16) low bytes of w at p, which is aligned to nbytes.
@@ -190,15 +196,18 @@ __device__ __forceinline__ void store_code_bytes(uint8_t* p, uint4 w, int nbytes
 
 // Writes the lane's codes and (group leaders) parameters of token row `slot`
 // into a page sub-block in global memory: [P][code_bytes] then
-// [P][param_row_bytes].
+// [P][param_row_bytes] (KIND, PT as for quantize_row).
+template <int KIND = -1, int PT = -1>
 __device__ __forceinline__ void store_row(const RowCodes& r, const PoolLayout& L, uint8_t* sub, int slot,
                                           int lane) {
   constexpr int P = 16;
+  const int kind = KIND >= 0 ? KIND : L.kind;
+  const int param = PT >= 0 ? PT : L.param;
   store_code_bytes(sub + slot * L.code_bytes + lane * r.nbytes, r.w, r.nbytes);
   uint8_t* prow = sub + P * L.code_bytes + slot * L.param_row_bytes;
   if (r.leader) {
-    store_param(prow + param_scale_offset(L, r.group), L.param, r.scale);
-    if (L.kind == KVQ_AFFINE_INT4) store_param(prow + param_bias_offset(L, r.group), L.param, r.bias);
+    store_param(prow + param_scale_offset<KIND, PT>(L, r.group), param, r.scale);
+    if (kind == KVQ_AFFINE_INT4) store_param(prow + param_bias_offset<PT>(L, r.group), param, r.bias);
   }
 }
 
