@@ -154,8 +154,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv") \
-            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/kvq_clocks_{os.getpid()}.csv"
+        # KVQ_CLOCKS_DIR keeps the samples where the caller wants them
+        out = os.environ.get("KVQ_CLOCKS_DIR")
+        self.path = os.path.join(out, f"clocks_gpu{gpu_index}.csv") if out and os.path.isdir(out) \
+            else f"/tmp/kvq_clocks_{os.getpid()}.csv"
 
     def start(self):
         try:

@@ -11,7 +11,7 @@ from int8_quantized_paged_gb300 import kvq
 from int8_quantized_paged_gb300.cache import LayerCache
 from oracle import kvq_oracle as O
 
-TOL = 2e-3            # max row-relative error of outputs (spec bound)
+TOL = 2e-3            # max row-relative error of outputs (the required bound)
 P = 16
 
 _ORACLE_ROPE = {}
