@@ -126,7 +126,7 @@ static size_t tc_ring_bytes(const kvq_config& c) {
 // configuration (grid, shared memory, warps, cluster size) and the 16-token
 // blocks per CTA.
 static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens, int32_t window, TcLaunch fn,
-                         size_t ring, size_t pre, TcLaunchCfg* lc, int* cb_out) {
+                         size_t ring, size_t pre, TcLaunchCfg* lc, int* cb_out, int* recv_out) {
   const int G = c.n_heads / c.n_kv_heads;
   const int hd = c.head_dim;
   const int nt = G > 4 ? 2 : 1;
@@ -136,17 +136,14 @@ static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens,
   const int64_t max_ppw = 8;
   if (blocks > (int64_t)kMaxCluster * kClusterWarps * max_ppw || (int64_t)batch * c.n_kv_heads > 4 * num_sms())
     return false;
-  // the warps' merge, then the CTA's partial o [G][hd] and (m, l) [G]
-  size_t need = ((size_t)kClusterWarps * G * (hd + 2) + G) * sizeof(float);
-  need = ((need + 15) & ~(size_t)15) + (size_t)G * hd * sizeof(float) + (size_t)G * 2 * sizeof(float);
-  size_t smem = (size_t)kClusterWarps * ring + pre;
-  if (smem < need) smem = need;
-  // One CTA per SM: with two, some SMs hold two CTAs of a cluster while others
-  // idle, and those CTAs finish last (measured: a smaller cluster at one CTA
-  // per SM is faster than 16 CTAs placed two to an SM).
-  if (smem < smem_per_sm() / 2 + 1) smem = smem_per_sm() / 2 + 1;
-  smem = (smem + 15) & ~(size_t)15;
-  if (smem > 200 * 1024) return false;
+  // The page rings and the query's staging, or the warps' merge that reuses
+  // them; then the receive buffers of the combine, which peers write while
+  // this CTA may still be in its loop.
+  size_t base = (size_t)kClusterWarps * ring + pre;
+  const size_t merge = ((size_t)kClusterWarps * G * (hd + 2) + G) * sizeof(float);
+  if (base < merge) base = merge;
+  base = (base + 15) & ~(size_t)15;
+  if (base + tc_recv_bytes(G, hd, kMaxCluster) > 200 * 1024) return false;
   int64_t hi = (blocks + kClusterWarps - 1) / kClusterWarps;   // one page per warp
   if (hi > kMaxCluster) hi = kMaxCluster;
   const int64_t lo = (blocks + kClusterWarps * max_ppw - 1) / (kClusterWarps * max_ppw);
@@ -155,6 +152,12 @@ static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens,
     const int64_t cb = (blocks + want - 1) / want;
     const int64_t nc = (blocks + cb - 1) / cb;
     if (nc != want) continue;   // the same split as a smaller cluster
+    // One CTA per SM: with two, some SMs hold two CTAs of a cluster while
+    // others idle, and those CTAs finish last (measured: a smaller cluster at
+    // one CTA per SM is faster than 16 CTAs placed two to an SM).
+    size_t smem = base + tc_recv_bytes(G, hd, (int)nc);
+    if (smem < smem_per_sm() / 2 + 1) smem = smem_per_sm() / 2 + 1;
+    smem = (smem + 15) & ~(size_t)15;
     TcLaunchCfg q = *lc;
     q.grid = dim3((unsigned)nc, c.n_kv_heads, batch);
     q.smem = smem;
@@ -163,6 +166,7 @@ static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens,
     if (max_active_clusters(fn, none, hd, nt, tc_ng(c), q) >= batch * c.n_kv_heads) {
       *lc = q;
       *cb_out = (int)cb;
+      *recv_out = (int)base;
       return true;
     }
   }
@@ -332,6 +336,7 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     t.kp_bytes = cfg->page_size * a.kl.param_row_bytes;
     t.vp_bytes = cfg->page_size * a.vl.param_row_bytes;
     t.cluster = 0;
+    t.recv_off = 0;
     const int nt = G > 4 ? 2 : 1;
     const int hd = cfg->head_dim;
     const int ng = tc_ng(*cfg);   // scale groups per head (K and V alike)
@@ -349,10 +354,11 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     lc.stream = stream;
     lc.pdl = pdl_enabled();
 
-    int cb = 0;
-    if (chunk_tokens == 0 && pick_cluster(*cfg, batch, max_tokens, window, fn, ring, pre, &lc, &cb)) {
+    int cb = 0, recv = 0;
+    if (chunk_tokens == 0 && pick_cluster(*cfg, batch, max_tokens, window, fn, ring, pre, &lc, &cb, &recv)) {
       t.cluster = lc.cluster;
       t.blocks_per_chunk = cb;
+      t.recv_off = recv;
       return fn(t, hd, nt, ng, lc);
     }
 
@@ -433,9 +439,9 @@ extern "C" int32_t kvq_decode_cluster_ctas(const kvq_config* cfg, int32_t batch,
   const int G = cfg->n_heads / cfg->n_kv_heads;
   const int64_t max_tokens = window > 0 ? window : (int64_t)max_pages_per_seq * cfg->page_size;
   TcLaunchCfg lc{};
-  int cb = 0;
+  int cb = 0, recv = 0;
   const bool on = pick_cluster(*cfg, batch, max_tokens, window, tc_launcher(*cfg), tc_ring_bytes(*cfg),
-                               tc_pre_bytes(cfg->head_dim, G > 4 ? 2 : 1, tc_ng(*cfg)), &lc, &cb);
+                               tc_pre_bytes(cfg->head_dim, G > 4 ? 2 : 1, tc_ng(*cfg)), &lc, &cb, &recv);
   return on ? lc.cluster : 0;
 }
 

@@ -69,12 +69,21 @@ struct TcArgs {
   int32_t kc_bytes, vc_bytes, kp_bytes, vp_bytes;  // code and scale bytes of a page (one kv head)
   int32_t cluster;           // 0: split-K partials through the workspace; else CTAs per
                              // thread-block cluster (= gridDim.x), combined in shared memory
+  int32_t recv_off;          // cluster mode: byte offset of the receive buffers (past every
+                             // other use of shared memory; tc_recv_bytes after it)
 };
 
 constexpr int kWarps = 4;                 // warps per CTA, split-K through the workspace
 constexpr int kTcThreads = 32 * kWarps;
 constexpr int kClusterWarps = 8;          // warps per CTA in the cluster mode
 constexpr int kMaxCluster = 16;           // CTAs per cluster (a non-portable size)
+// Cluster-mode receive buffers of a CTA: the (M, l) pair of every head of
+// every CTA of the cluster [kMaxCluster][G], then the partial o of this CTA's
+// slice of the G * hd outputs from every CTA [cluster][per].
+constexpr int kRecvMl = kMaxCluster * 8 * 8;
+inline size_t tc_recv_bytes(int G, int hd, int cluster) {
+  return kRecvMl + ((size_t)G * hd + cluster) * sizeof(float);
+}
 constexpr float kQScale = 256.0f;   // q is held x 2^8 in fp16 (hi/lo)
 constexpr float kWScale = 128.0f;   // w is held x 2^7 (w <= 2^8 * 2^7 < 65504)
 constexpr float kLazyMax = 8.0f;    // raise the running max only past +2^8
@@ -331,11 +340,14 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     }
     return;
   }
+  // cluster mode: this CTA has started; the wait before the first store into
+  // a peer's shared memory makes sure every peer has too
+  if constexpr (CL) tc::cluster_arrive_relaxed();
   const int blk_lo = lo / P, blk_hi = (L + P - 1) / P;
   const int nch = (blk_hi - blk_lo + CB - 1) / CB;
-  // In the cluster mode every CTA of the cluster reaches both cluster barriers
-  // below: a CTA past the sequence's last chunk reads no page and contributes
-  // an empty partial.
+  // In the cluster mode every CTA of the cluster reaches every cluster
+  // barrier below: a CTA past the sequence's last chunk reads no page and
+  // contributes an empty partial.
   if (chunk >= nch && !CL) return;
   const int cb0 = blk_lo + chunk * CB;
   const int ncb = chunk < nch ? min(CB, blk_hi - cb0) : 0;
@@ -1128,10 +1140,15 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   __syncthreads();
 
   const int64_t cidx = ((int64_t)b * a.n_kv_heads + kvh) * a.n_chunks + chunk;
-  // cluster mode: the CTA's merged partial stays in its own shared memory,
-  // o [G][HD] then (M, l) [G], after the warps' states
-  const uint32_t cpart = tc::smem_u32(smem) + (((uint32_t)(NW * G * HD + 2 * NW * G + G) * 4 + 15) & ~15u);
-  const uint32_t cml = cpart + 4 * G * HD;
+  // cluster mode: the CTA's merged partial goes straight into the receive
+  // buffers of the CTAs that combine it: output i to CTA i / per, and every
+  // head's (M, l) to every CTA
+  const int ncl = CL ? A.cluster : 1;
+  const int per = (G * HD + ncl - 1) / ncl;   // outputs combined per CTA
+  const uint32_t rml = tc::smem_u32(smem) + (uint32_t)A.recv_off;
+  const uint32_t rbo = rml + kRecvMl;
+  const int rank = CL ? (int)tc::cluster_rank() : 0;
+  if constexpr (CL) tc::cluster_wait();
   for (int i = tid; i < G * HD; i += NW * 32) {
     const int h = i / HD, d = i - h * HD;
     const float M = Mh[h];
@@ -1142,8 +1159,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       ls += lws[w2 * G + h];
     }
     if constexpr (CL) {
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(cpart + 4 * i), "f"(o) : "memory");
-      if (d == 0) asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(cml + 8 * h), "f"(M), "f"(ls) : "memory");
+      const int own = i / per;
+      tc::st_cluster_f(tc::cluster_addr(rbo + 4 * (rank * per + i - own * per), own), o);
+      if (d == 0)
+        for (int c = 0; c < ncl; ++c) tc::st_cluster_f2(tc::cluster_addr(rml + 8 * (rank * G + h), c), M, ls);
     } else if (nch == 1) {
       store_act(A.out, a.act, obase + i, ls > 0.f ? o / ls : 0.f);
     } else {
@@ -1155,18 +1174,14 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     }
   }
 
-  // ---- cluster mode: log-sum-exp combine over distributed shared memory.
-  // After the first cluster barrier every CTA's partial is visible to the
-  // cluster; CTA r then combines its slice of the G * HD outputs from the
-  // partials of all A.cluster CTAs, and the second barrier keeps every CTA's
-  // shared memory alive until the whole cluster is done reading it.
+  // ---- cluster mode: log-sum-exp combine.  After the cluster barrier every
+  // CTA's partials are in the receive buffers of the CTAs that combine them;
+  // CTA r combines outputs [r per, (r + 1) per) from its own shared memory and
+  // may exit: no CTA touches another's shared memory after the barrier.
   if constexpr (CL) {
     tc::cluster_barrier();
-    const int nc = A.cluster;
-    const int E = G * HD;
-    const int per = (E + nc - 1) / nc;
-    const int e0 = (int)tc::cluster_rank() * per;
-    const int e1 = min(E, e0 + per);
+    const int e0 = rank * per;
+    const int e1 = min(G * HD, e0 + per);
     for (int e = e0 + tid; e < e1; e += NW * 32) {
       const int h = e / HD;
       float2 ml[kMaxCluster];
@@ -1175,9 +1190,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       for (int c = 0; c < kMaxCluster; ++c) {
         ml[c] = make_float2(-INFINITY, 0.f);
         v[c] = 0.f;
-        if (c < nc) {
-          ml[c] = tc::ld_cluster_f2(tc::cluster_addr(cml + 8 * h, c));
-          v[c] = tc::ld_cluster_f(tc::cluster_addr(cpart + 4 * e, c));
+        if (c < ncl) {
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(ml[c].x), "=f"(ml[c].y) : "r"(rml + 8 * (c * G + h)));
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[c]) : "r"(rbo + 4 * (c * per + e - e0)));
         }
       }
       float mx = -INFINITY;
@@ -1194,7 +1209,6 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       }
       store_act(A.out, a.act, obase + e, den > 0.f ? num / den : 0.f);
     }
-    tc::cluster_barrier();
     return;
   }
   if (nch == 1) return;
