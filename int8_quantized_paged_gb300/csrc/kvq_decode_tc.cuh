@@ -1148,7 +1148,17 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   const uint32_t rml = tc::smem_u32(smem) + (uint32_t)A.recv_off;
   const uint32_t rbo = rml + kRecvMl;
   const int rank = CL ? (int)tc::cluster_rank() : 0;
-  if constexpr (CL) tc::cluster_wait();
+  if constexpr (CL) {
+    tc::cluster_wait();
+    // the (M, l) of head h to CTA c: one store for each of ncl * G threads
+    if (tid < ncl * G) {
+      const int h = tid % G, c = tid / G;
+      float ls = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < NW; ++w2) ls += lws[w2 * G + h];
+      tc::st_cluster_f2(tc::cluster_addr(rml + 8 * (rank * G + h), c), Mh[h], ls);
+    }
+  }
   for (int i = tid; i < G * HD; i += NW * 32) {
     const int h = i / HD, d = i - h * HD;
     const float M = Mh[h];
@@ -1161,8 +1171,6 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     if constexpr (CL) {
       const int own = i / per;
       tc::st_cluster_f(tc::cluster_addr(rbo + 4 * (rank * per + i - own * per), own), o);
-      if (d == 0)
-        for (int c = 0; c < ncl; ++c) tc::st_cluster_f2(tc::cluster_addr(rml + 8 * (rank * G + h), c), M, ls);
     } else if (nch == 1) {
       store_act(A.out, a.act, obase + i, ls > 0.f ? o / ls : 0.f);
     } else {
