@@ -306,3 +306,85 @@ def test_append_codes_at_rounding_ties(name, over):
     O.append(spec, pools, k, v, np.zeros(n, np.int64), np.arange(n), bt, 0, oracle_rope(spec.head_dim, spec.rope_base, n + 1))
     assert np.array_equal(cache.k_pool.cpu().numpy(), pools["k"])
     assert np.array_equal(cache.v_pool.cpu().numpy(), pools["v"])
+
+
+# ---------------------------------------------------------------- bf16 activations
+
+def _round_bf16(x: np.ndarray) -> np.ndarray:
+    """x rounded once to bf16, as fp32 (input preparation: both sides read these values)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+class _Bf16Case(Case):
+    """A Case with bf16 activations: rows and queries drawn in fp32 and rounded to
+    bf16 once; the device gets the bf16 tensors, the oracle the same values."""
+
+    def _draws(self) -> dict:
+        return dict(self.w, act="f32")
+
+    def _fill_gpu(self):
+        dev = self.cache.device
+        for b, L in enumerate(self.lens):
+            k = _round_bf16(wl.kv_rows(self._draws(), b, "k", int(L)))
+            v = _round_bf16(wl.kv_rows(self._draws(), b, "v", int(L)))
+            if b in self.oracle_seqs:
+                self.rows[b] = (k, v)
+            for s, e in self._chunks(int(L)):
+                self.cache.append(torch.from_numpy(k[s:e]).to(dev).to(torch.bfloat16),
+                                  torch.from_numpy(v[s:e]).to(dev).to(torch.bfloat16),
+                                  torch.arange(s, e, dtype=torch.int32, device=dev),
+                                  torch.full((e - s,), b, dtype=torch.int32, device=dev))
+        torch.cuda.synchronize()
+
+    def queries(self, step: int = 0) -> np.ndarray:
+        return _round_bf16(wl.queries(dict(self._draws(), batch=self.B), step=step))
+
+    def gpu_decode(self, q: np.ndarray, chunk_tokens: int = 0, window: int = 0, lens=None, stream=None):
+        dev = self.cache.device
+        qt = torch.from_numpy(q).to(dev).to(torch.bfloat16)
+        out = torch.full_like(qt, float("nan"))
+        ws = self.cache.workspace(self.B, chunk_tokens, window)
+        lt = torch.from_numpy(self.lens).to(dev)
+        if window:
+            self.cache.window_decode(qt, lt, out, ws, window, chunk_tokens)
+        else:
+            self.cache.decode(qt, lt, out, ws, chunk_tokens)
+        torch.cuda.synchronize()
+        return out.float().cpu().numpy().astype(np.float64)
+
+
+# The output is rounded once to bf16 (8 significant bits): up to 2^-8 of its
+# magnitude on top of the 2e-3 bound of the arithmetic before it.
+TOL_BF16_OUT = TOL + 2.0 ** -8
+
+
+@pytest.mark.parametrize("name", ["llama8b", "gemma_mix", "long_mixed"])
+def test_bf16_activations_match_oracle(name):
+    """bf16 q, K/V rows and output: pools bytewise, outputs within TOL_BF16_OUT,
+    for the plain decode (both launch modes) and the fused step."""
+    c = _Bf16Case(wl.workload(name, batch=2, act="bf16"), [700, 33])
+    k, v = c.gpu_pools()
+    assert np.array_equal(k, c.pools["k"]) and np.array_equal(v, c.pools["v"])
+    q = c.queries()
+    ref = c.oracle_decode(q)
+    for chunk in (0, 64):
+        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), ref) <= TOL_BF16_OUT, chunk
+    # the fused step: new rows at L - 1
+    dev = c.cache.device
+    k_new = _round_bf16(wl.new_rows(c._draws(), "k", c.B, step=1))
+    v_new = _round_bf16(wl.new_rows(c._draws(), "v", c.B, step=1))
+    q1 = c.queries(step=1)
+    pos = (c.lens - 1).astype(np.int32)
+    qt = torch.from_numpy(q1).to(dev).to(torch.bfloat16)
+    out = torch.full_like(qt, float("nan"))
+    c.cache.append_decode(qt, torch.from_numpy(k_new).to(dev).to(torch.bfloat16),
+                          torch.from_numpy(v_new).to(dev).to(torch.bfloat16), torch.from_numpy(pos).to(dev),
+                          torch.from_numpy(c.lens).to(dev), out, c.cache.workspace(c.B))
+    torch.cuda.synchronize()
+    assert c.cache.status_bits() == 0
+    s = c.spec
+    O.append(s, c.pools, k_new, v_new, np.arange(c.B), pos, c.bt, 0, oracle_rope(s.head_dim, s.rope_base, c.rope_max))
+    k, v = c.gpu_pools()
+    assert np.array_equal(k, c.pools["k"]) and np.array_equal(v, c.pools["v"])
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert max_row_err(got, c.oracle_decode(q1)) <= TOL_BF16_OUT
