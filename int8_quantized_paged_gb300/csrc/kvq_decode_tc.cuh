@@ -998,9 +998,15 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 
   int s = 0;   // slot of page k: k % D
   int k = 0;
-  if constexpr (CL) {
-    // Two pages a step: their Q.K chains are independent, one softmax update
-    // covers 32 tokens, and the wait and the loop control come once per pair.
+  // Two pages a step where the page's code is small (4-bit K and V, head_dim
+  // <= 128): their Q.K chains are independent, one softmax update covers 32
+  // tokens, and the wait and the loop control come once per pair.  The step
+  // doubles the unrolled page code, so for f16, 8-bit or head_dim-256 pages the
+  // one-page loop, which stays in the instruction cache, is faster (measured:
+  // f16 llama8b shape 11.2 -> 10.2 us per layer, gemma mix +1 %; the 4-bit
+  // llama8b shape 2.6 % slower without the step).
+  constexpr bool PAIR_STEP = CL && !F16 && !K8 && !V8 && HD <= 128;
+  if constexpr (PAIR_STEP) {
     // Pages k, k+1 landed: at most D - 2 younger commit groups pending.
 #pragma unroll 1
     for (; k + 1 < n_local; k += 2) {
