@@ -1017,9 +1017,14 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         place_app(k == k_app ? s : s1);
         __syncwarp();
       }
-      if (((valid >> s) & (valid >> s1) & 1u) != 0) {
-        const int ta = tok0(k), tb1 = tok0(k + 1);
-        const bool ea = is_edge(ta), eb = is_edge(tb1);
+      {
+        // A page with a bad id (no copy: its slot holds stale data) goes
+        // through as an edge page whose rows all start at L, so every row is
+        // masked: its scores -inf, its V scales 0 (4-bit codes convert to
+        // finite values whatever the bytes).
+        const bool oka = ((valid >> s) & 1u) != 0, okb = ((valid >> s1) & 1u) != 0;
+        const int ta = oka ? tok0(k) : L, tb1 = okb ? tok0(k + 1) : L;
+        const bool ea = !oka || is_edge(ta), eb = !okb || is_edge(tb1);
         float sa[NT][2], sb[NT][2], pa[NT][2], pb[NT][2], bm[NT];
         page_scores(s, ta, ea, sa);
         page_scores(s1, tb1, eb, sb);
@@ -1030,9 +1035,6 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         probs(sb, pb);
         page_pv(s, ta, ea, pa);
         page_pv(s1, tb1, eb, pb);
-      } else {   // a page with a bad id: the other one alone
-        if ((valid >> s) & 1u) one_page(k, s);
-        if ((valid >> s1) & 1u) one_page(k + 1, s1);
       }
       // both slots are free once every lane is done reading them
       __syncwarp();

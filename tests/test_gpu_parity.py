@@ -156,6 +156,7 @@ def test_device_status_flags_bad_inputs():
     got = c.gpu_decode(q)
     assert c.cache.status_bits() & kvq.DEV_BAD_PAGE
     assert max_row_err(got, ref, seqs=[0, 2]) <= TOL         # other sequences unaffected
+    assert np.all(np.isfinite(got[1]))                         # the bad page's rows are left out
     c.cache.set_table(c.bt)
     # a length past the table's capacity gives a zero row and a flag
     kvq.clear_device_status(c.cache.status)
