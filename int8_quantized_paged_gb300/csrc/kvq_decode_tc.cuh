@@ -1196,34 +1196,47 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   // may exit: no CTA touches another's shared memory after the barrier.
   if constexpr (CL) {
     tc::cluster_barrier();
+    // four threads an output, sources c = part, part + 4, ... each; the four
+    // lanes of a group are consecutive, so xor 1 and 2 reach the others
     const int e0 = rank * per;
     const int e1 = min(G * HD, e0 + per);
-    for (int e = e0 + tid; e < e1; e += NW * 32) {
-      const int h = e / HD;
-      float2 ml[kMaxCluster];
-      float v[kMaxCluster];
+    const int part = tid & 3;
+    for (int base = e0; base < e1; base += NW * 8) {   // the same trip count for every thread
+      const int e = base + (tid >> 2);
+      const bool ok = e < e1;
+      const int h = (ok ? e : e0) / HD;
+      constexpr int NS = kMaxCluster / 4;
+      float2 ml[NS];
+      float v[NS];
 #pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c) {
-        ml[c] = make_float2(-INFINITY, 0.f);
-        v[c] = 0.f;
-        if (c < ncl) {
-          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(ml[c].x), "=f"(ml[c].y) : "r"(rml + 8 * (c * G + h)));
-          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[c]) : "r"(rbo + 4 * (c * per + e - e0)));
+      for (int j = 0; j < NS; ++j) {
+        const int c = part + 4 * j;
+        ml[j] = make_float2(-INFINITY, 0.f);
+        v[j] = 0.f;
+        if (ok && c < ncl) {
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(ml[j].x), "=f"(ml[j].y) : "r"(rml + 8 * (c * G + h)));
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[j]) : "r"(rbo + 4 * (c * per + e - e0)));
         }
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c) mx = fmaxf(mx, ml[c].x);
+      for (int j = 0; j < NS; ++j) mx = fmaxf(mx, ml[j].x);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       float num = 0.f, den = 0.f;
       if (mx != -INFINITY) {
 #pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c) {
-          const float wt = exp2f(ml[c].x - mx);   // 0 for an empty partial (-inf)
-          num = fmaf(wt, v[c], num);
-          den = fmaf(wt, ml[c].y, den);
+        for (int j = 0; j < NS; ++j) {
+          const float wt = tc::ex2(ml[j].x - mx);   // 0 for an empty partial (-inf)
+          num = fmaf(wt, v[j], num);
+          den = fmaf(wt, ml[j].y, den);
         }
       }
-      store_act(A.out, a.act, obase + e, den > 0.f ? num / den : 0.f);
+      num += __shfl_xor_sync(0xffffffffu, num, 1);
+      den += __shfl_xor_sync(0xffffffffu, den, 1);
+      num += __shfl_xor_sync(0xffffffffu, num, 2);
+      den += __shfl_xor_sync(0xffffffffu, den, 2);
+      if (ok && part == 0) store_act(A.out, a.act, obase + e, den > 0.f ? num / den : 0.f);
     }
     return;
   }
