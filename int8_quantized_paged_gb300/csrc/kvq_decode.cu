@@ -133,7 +133,10 @@ static bool pick_cluster(const kvq_config& c, int32_t batch, int64_t max_tokens,
   if (!cluster_enabled() || batch < 1 || !tc_cluster_shape(hd, nt)) return false;
   // blocks of the longest context (a window may start mid-page)
   const int64_t blocks = (max_tokens + c.page_size - 1) / c.page_size + (window > 0 ? 1 : 0);
-  const int64_t max_ppw = 8;
+  // pages per warp at most: 8, or 12 at head_dim 256, where a 16K-token global
+  // layer in 12-CTA clusters (10.7 pages per warp) beat the workspace mode
+  // (bench step of the sliding+global mix 669 -> 691 GB/s)
+  const int64_t max_ppw = hd == 256 ? 12 : 8;
   if (blocks > (int64_t)kMaxCluster * kClusterWarps * max_ppw || (int64_t)batch * c.n_kv_heads > 4 * num_sms())
     return false;
   // The page rings and the query's staging, or the warps' merge that reuses
