@@ -183,6 +183,18 @@ def test_round_trip_bound():
         # the largest element of each group gets the extreme code
         qmax = 2 ** (bits - 1) - 1
         assert np.all(np.max(np.abs(c.reshape(200, 4, 32)), axis=-1) == qmax)
+    # the /7.5 codec: max|x| / scale = 7.5 up to the scale's rounding, so the
+    # largest element lands on the clamp at +7 (or on -8) with an error of half
+    # a step at most, the fp32 rounding of the scale aside (7.5 * 2^-24 of it)
+    x = (rng.standard_normal((200, 128)) * rng.uniform(0.01, 50, (200, 1))).astype(np.float32)
+    c, s, _ = O.quantize("shimmy4", x, 32, "f32")
+    xh = O.dequantize(c, s, None, 32)
+    err = np.abs(x.astype(np.float64) - xh).reshape(200, 4, 32)
+    assert np.all(err <= (s.astype(np.float64) / 2 * (1 + 2.0 ** -19))[..., None])
+    assert c.min() >= -8 and c.max() <= 7
+    # the largest element's quotient is 7.5 up to the scale's rounding: code 7
+    # (from +-7.5 down, or +8 clamped) or -8
+    assert np.all(np.max(np.abs(c.reshape(200, 4, 32).astype(np.int64)), axis=-1) >= 7)
     # affine with bf16-exact min/max and an exact step: error <= scale/2
     mn = np.float32(-1.5)
     xs = (mn + np.arange(64, dtype=np.float32) * np.float32(15 / 63)).astype(np.float32)
