@@ -1,6 +1,9 @@
 // Tensor-core split-K GQA decode attention over a paged, group-quantized KV
-// cache, with the log-sum-exp combine fused into the last CTA of each
-// (sequence, kv head).
+// cache, with the log-sum-exp combine fused in: by the last CTA of each
+// (sequence, kv head) through a global workspace, or, for a few short
+// sequences, inside a thread-block cluster per (sequence, kv head) whose CTAs
+// push their partials into each other's shared memory.  The same kernel can
+// also write the step's new K/V row first (the fused append).
 //
 // Method: softmax(q K^T * s) V straight from the packed codes through a block
 // table ([airllm] §2.2: dequantize inside the kernel after the load, with no
@@ -44,6 +47,8 @@
 // Each warp keeps its own (m, l, O); the warps merge through shared memory at
 // the end.  G = 8 (NT = 2) puts the 8 heads in the 8 columns of one tile and
 // runs the high and the low parts as two passes into the same accumulators.
+// 4-bit codes are symmetric (two's complement), affine (unsigned) or offset
+// binary (stored as code + 8); unquantised f16 rows go to the MMAs as loaded.
 #pragma once
 
 #include <cuda.h>
