@@ -424,6 +424,82 @@ def test_f16_kv_layout_and_brute_force_attention():
         assert np.allclose(got[0, h], ref, rtol=1e-12, atol=1e-12)
 
 
+def _rotate_closed_form(x, pos, base, mode):
+    """The rotation written out from its definition, in pure Python:
+    theta_i = base^(-2i/hd), pair i rotated by pos * theta_i; pairs (2i, 2i+1),
+    or (i, i + hd/2) for NeoX ([Shimmy] §2.2/§2.3, [Fieldfare] "量化和精度")."""
+    hd = len(x)
+    out = [float(v) for v in x]
+    for i in range(hd // 2):
+        a, b = (2 * i, 2 * i + 1) if mode == "normal" else (i, i + hd // 2)
+        ang = pos * base ** (-2.0 * i / hd)
+        c, s = math.cos(ang), math.sin(ang)
+        out[a] = float(x[a]) * c - float(x[b]) * s
+        out[b] = float(x[a]) * s + float(x[b]) * c
+    return out
+
+
+@pytest.mark.parametrize("mode", ["normal", "neox"])
+def test_rope_positions_against_brute_force(mode):
+    """Where the rotation is applied ([Shimmy] §2.3: q and k are rotated;
+    [Fieldfare] "KV Cache 的双布局设计": K is rotated before it is cached, V is
+    not): key t at its own position t, the decode query at L - 1.  With the
+    unquantised f16 kind (reading R8) no code intervenes, so the oracle's
+    append + decode must equal brute-force attention over keys rotated by the
+    closed form and rounded to fp16 once.  The same brute force with the keys
+    one position late, or the query one position late, must differ widely, so a
+    slip in either position fails here."""
+    hd, base, L = 16, 100.0, 23
+    spec = O.Spec(n_heads=4, n_kv_heads=2, head_dim=hd, page_size=16, k_kind="f16", v_kind="f16",
+                  k_group=hd, v_group=hd, k_param="f32", v_param="f32", act="f32", rope=mode,
+                  rope_base=base)
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((L, 2, hd)).astype(np.float32)
+    v = rng.standard_normal((L, 2, hd)).astype(np.float32)
+    q = rng.standard_normal((1, 4, hd)).astype(np.float32)
+    bt = np.array([[3, 0]], np.int32)
+    pools = {w: np.zeros(4 * O.page_bytes(spec, w), np.uint8) for w in ("k", "v")}
+    O.append(spec, pools, k, v, np.zeros(L, np.int64), np.arange(L), bt, 0, O.rope_table(hd, base, L + 1))
+    got = O.decode(spec, q, pools, bt, np.array([L]))
+    alpha = 1.0 / math.sqrt(hd)
+
+    def brute(k_shift, q_shift):
+        o = np.zeros((4, hd))
+        for h in range(4):
+            kv = h // 2
+            K = [np.float16(_rotate_closed_form(k[t, kv], t + k_shift, base, mode)).astype(np.float64).tolist()
+                 for t in range(L)]
+            V = [v[t, kv].astype(np.float16).astype(np.float64).tolist() for t in range(L)]
+            qr = _rotate_closed_form(q[0, h], L - 1 + q_shift, base, mode)
+            o[h] = _brute_attend(qr, K, V, alpha)
+        return o
+
+    ref = brute(0, 0)
+    scale = np.max(np.abs(ref))
+    # fp32 rotation with the fp32 table before the fp16 rounding, against the
+    # fp64 closed form: at most a one-ulp fp16 difference in a few elements
+    assert np.max(np.abs(got[0] - ref)) <= 1e-3 * scale
+    for ks, qs in ((1, 0), (0, 1), (-1, 0), (0, -1)):
+        assert np.max(np.abs(brute(ks, qs) - ref)) >= 3e-2 * scale, (ks, qs)
+
+
+def test_rope_scores_depend_on_relative_position():
+    """A rotation pair at positions (p, t) gives the same fp64 score as at
+    (p + d, t + d): the scores see only p - t.  Moving the query alone changes
+    them."""
+    hd, base = 32, 500000.0
+    rng = np.random.default_rng(5)
+    q, kk = rng.standard_normal(hd), rng.standard_normal(hd)
+    for mode in ("normal", "neox"):
+        for p, t in ((0, 0), (7, 3), (8191, 100), (65535, 65000)):
+            s0 = O.rotate_f64(q, p, hd, base, mode) @ O.rotate_f64(kk, t, hd, base, mode)
+            for d in (1, 13, 4096):
+                s1 = O.rotate_f64(q, p + d, hd, base, mode) @ O.rotate_f64(kk, t + d, hd, base, mode)
+                assert abs(s1 - s0) <= 1e-12 * max(1.0, abs(s0)), (mode, p, t, d)
+            s2 = O.rotate_f64(q, p + 1, hd, base, mode) @ O.rotate_f64(kk, t, hd, base, mode)
+            assert abs(s2 - s0) > 1e-3, (mode, p, t)
+
+
 def test_shimmy_codec_hand_worked_and_brute_force():
     """[Shimmy] §3.2 quantize_head_vector (reading R9): scale = max|x| / 7.5,
     code = clamp(round(x / scale), -8, 7) rounding half away from zero, stored
@@ -493,8 +569,9 @@ def test_row_rel_error_rule():
     assert O.row_rel_error(ref, ref)[0] == 0
     got = ref + np.array([[1e-3, 0, 0, 0]])
     assert math.isclose(O.row_rel_error(got, ref)[0], 1e-3)
-    got = ref + np.array([[0, 0, 1e-5, 0]])                # near-zero element uses the row floor (1 %)
+    got = ref + np.array([[0, 0, 1e-6, 0]])                # near-zero element uses the row floor (0.1 %)
     assert math.isclose(O.row_rel_error(got, ref)[0], 1e-3)
+    assert math.isclose(O.row_rel_error(got, ref, floor=1e-2)[0], 1e-4)   # an explicit wider floor
     got = ref + np.array([[0, 2e-4, 0, 0]])                # 0.5 is above the floor: relative to itself
     assert math.isclose(O.row_rel_error(got, ref)[0], 4e-4)
     assert math.isclose(O.row_norm_error(got, ref)[0], 2e-4)
