@@ -116,10 +116,31 @@ class Case:
                         seqs=self.oracle_seqs if seqs is None else seqs)
 
 
-def max_row_err(got, ref, seqs=None):
+FLOOR = 1e-3          # row floor of the output comparison (0.1 % of the row's largest magnitude)
+
+
+def floor_for(w: dict) -> float:
+    """Row floor for a workload's outputs.
+
+    The absolute fp32 error of a score grows with attn_scale * sum_d |q_d k_d|,
+    about attn_scale * head_dim for N(0,1) rows, while the default scale
+    1/sqrt(head_dim) keeps that at sqrt(head_dim).  So the floor is 0.1 %
+    times attn_scale * sqrt(head_dim) (at least 1), and at most 1 %: only a
+    layer with a raised score scale (attention scale 1.0, as the sliding +
+    global mix uses) gets more than 0.1 %.
+    """
+    alpha = float(w.get("attn_scale", 0.0))
+    if alpha <= 0.0:
+        return FLOOR
+    return min(1e-2, FLOOR * max(1.0, alpha * float(w["head_dim"]) ** 0.5))
+
+
+def max_row_err(got, ref, seqs=None, floor=FLOOR):
+    """The larger of the max row-relative error (with the given row floor) and
+    the max normwise error, over the rows of the selected sequences."""
     if seqs is not None:
         got, ref = got[list(seqs)], ref[list(seqs)]
-    return float(np.max(O.row_rel_error(got, ref)))
+    return float(max(np.max(O.row_rel_error(got, ref, floor=floor)), np.max(O.row_norm_error(got, ref))))
 
 
 def pages_of(case: Case, b: int):

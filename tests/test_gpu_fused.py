@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import kvq_workloads as wl
-from gpu_cases import TOL, Case, max_row_err, oracle_rope
+from gpu_cases import TOL, Case, floor_for, max_row_err, oracle_rope
 from int8_quantized_paged_gb300 import kvq
 from oracle import kvq_oracle as O
 
@@ -82,7 +82,7 @@ def test_fused_step_matches_oracle_and_separate_calls(key, chunk):
     k, v = c.gpu_pools()
     assert np.array_equal(k, c.pools["k"])
     assert np.array_equal(v, c.pools["v"])
-    assert max_row_err(got, c.oracle_decode(q)) <= TOL
+    assert max_row_err(got, c.oracle_decode(q), floor=floor_for(c.w)) <= TOL
     # the plain decode over the pools the fused call wrote gives the same bits
     assert np.array_equal(got, c.gpu_decode(q, chunk_tokens=chunk))
     # the separate append of the same rows rewrites the same bytes
@@ -114,7 +114,7 @@ def test_row_past_the_attended_length_is_written_not_attended():
     k, v = c.gpu_pools()
     assert np.array_equal(k, c.pools["k"]) and np.array_equal(v, c.pools["v"])
     ref = O.decode(c.spec, q, c.pools, c.bt, lens)
-    assert max_row_err(got, ref) <= TOL
+    assert max_row_err(got, ref, floor=floor_for(c.w)) <= TOL
 
 
 def test_bad_position_flags_and_skips_the_row():
@@ -125,7 +125,7 @@ def test_bad_position_flags_and_skips_the_row():
     assert c.cache.status_bits() == kvq.DEV_BAD_POS
     k, v = c.gpu_pools()
     assert np.array_equal(k, before_k) and np.array_equal(v, before_v)
-    assert max_row_err(got, c.oracle_decode(q)) <= TOL   # the decode itself is unaffected
+    assert max_row_err(got, c.oracle_decode(q), floor=floor_for(c.w)) <= TOL   # the decode itself is unaffected
 
 
 def test_fused_argument_checks():
@@ -177,7 +177,7 @@ def test_fused_window_step_matches_oracle(L, chunk, name):
                                                                                       c.rope_max))
     k, v = c.gpu_pools()
     assert np.array_equal(k, c.pools["k"]) and np.array_equal(v, c.pools["v"])
-    assert max_row_err(got, c.oracle_decode(q, window=1024)) <= TOL
+    assert max_row_err(got, c.oracle_decode(q, window=1024), floor=floor_for(c.w)) <= TOL
     assert np.array_equal(got, c.gpu_decode(q, chunk_tokens=chunk, window=1024))
 
 

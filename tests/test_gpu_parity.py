@@ -1,15 +1,17 @@
 """GPU path (through the C ABI) against the CPU oracle on the same seeded inputs.
 
 Codes and scales: bytewise equal pools.  Outputs: max row-relative error
-<= 2e-3 (elements below 1 % of the row's largest magnitude compare against
-that floor) and max normwise error <= 2e-3.  Sizes span several chunks, several pages and ragged tails.
+<= 2e-3 and max normwise error <= 2e-3 in every decode check.  Elements below
+0.1 % of the row's largest magnitude compare against that floor; layers with
+a raised score scale pass a wider floor (gpu_cases.floor_for).  Sizes span
+several chunks, several pages and ragged tails.
 """
 import numpy as np
 import pytest
 import torch
 
 import kvq_workloads as wl
-from gpu_cases import TOL, Case, max_row_err, oracle_rope
+from gpu_cases import TOL, Case, floor_for, max_row_err, oracle_rope
 from int8_quantized_paged_gb300 import kvq
 from int8_quantized_paged_gb300.cache import LayerCache
 from oracle import kvq_oracle as O
@@ -44,7 +46,9 @@ def test_normwise_error_small():
     c = Case(w, [3001, 5])
     q = c.queries()
     got = c.gpu_decode(q)
-    assert float(np.max(O.row_norm_error(got, c.oracle_decode(q)))) <= TOL
+    ref = c.oracle_decode(q)
+    assert float(np.max(O.row_norm_error(got, ref))) <= TOL
+    assert max_row_err(got, ref, floor=floor_for(c.w)) <= TOL
 
 
 def _case(name, **kw):
@@ -71,7 +75,7 @@ def test_decode_matches_oracle(case, chunk):
     ref = case.oracle_decode(q)
     got = case.gpu_decode(q, chunk_tokens=chunk)
     assert np.all(np.isfinite(got))
-    assert max_row_err(got, ref) <= TOL
+    assert max_row_err(got, ref, floor=floor_for(case.w)) <= TOL
     for b, L in enumerate(case.lens):
         if L == 0:
             assert np.all(got[b] == 0)
@@ -85,7 +89,7 @@ def test_chunk_count_invariance(case):
     c = case.gpu_decode(q)
     ref = case.oracle_decode(q)
     for x in (a, b, c):
-        assert max_row_err(x, ref) <= TOL
+        assert max_row_err(x, ref, floor=floor_for(case.w)) <= TOL
     assert np.max(np.abs(a - c)) <= 4e-3 * max(1e-6, np.max(np.abs(ref)))
 
 
@@ -99,7 +103,7 @@ def test_window_ring_matches_oracle(L):
     ref = c.oracle_decode(q, window=1024)
     for chunk in (0, 64):
         got = c.gpu_decode(q, chunk_tokens=chunk, window=1024)
-        assert max_row_err(got, ref) <= TOL, (L, chunk)
+        assert max_row_err(got, ref, floor=floor_for(c.w)) <= TOL, (L, chunk)
 
 
 def test_window_small_ring_other_codec():
@@ -109,7 +113,7 @@ def test_window_small_ring_other_codec():
     q = c.queries()
     ref = c.oracle_decode(q, window=40)
     got = c.gpu_decode(q, window=40)
-    assert max_row_err(got, ref) <= TOL
+    assert max_row_err(got, ref, floor=floor_for(c.w)) <= TOL
 
 
 def test_length_one_returns_its_value():
@@ -118,7 +122,7 @@ def test_length_one_returns_its_value():
     q = c.queries()
     got = c.gpu_decode(q)
     ref = c.oracle_decode(q)                       # = the dequantized v of token 0
-    assert max_row_err(got, ref) <= TOL
+    assert max_row_err(got, ref, floor=floor_for(c.w)) <= TOL
 
 
 def test_non_default_stream_and_isolation():
@@ -129,7 +133,7 @@ def test_non_default_stream_and_isolation():
     with torch.cuda.stream(s):
         before = c.gpu_decode(q, stream=s)
     ref = c.oracle_decode(q)
-    assert max_row_err(before, ref) <= TOL
+    assert max_row_err(before, ref, floor=floor_for(c.w)) <= TOL
     # grow sequence 0 by one token: sequence 1's output must not change at all
     c.cache.reserve(0, 301)
     c.cache.sync_table()
@@ -155,14 +159,14 @@ def test_device_status_flags_bad_inputs():
     kvq.clear_device_status(c.cache.status)
     got = c.gpu_decode(q)
     assert c.cache.status_bits() & kvq.DEV_BAD_PAGE
-    assert max_row_err(got, ref, seqs=[0, 2]) <= TOL         # other sequences unaffected
+    assert max_row_err(got, ref, seqs=[0, 2], floor=floor_for(c.w)) <= TOL   # other sequences unaffected
     assert np.all(np.isfinite(got[1]))                         # the bad page's rows are left out
     c.cache.set_table(c.bt)
     # a length past the table's capacity gives a zero row and a flag
     kvq.clear_device_status(c.cache.status)
     got = c.gpu_decode(q, lens=[40, 10 ** 6, 40])
     assert c.cache.status_bits() & kvq.DEV_BAD_LEN
-    assert np.all(got[1] == 0) and max_row_err(got, ref, seqs=[0, 2]) <= TOL
+    assert np.all(got[1] == 0) and max_row_err(got, ref, seqs=[0, 2], floor=floor_for(c.w)) <= TOL
     # append: a sequence id and a position outside the table are flagged and skipped
     kvq.clear_device_status(c.cache.status)
     k0 = c.cache.k_pool.clone()
@@ -195,7 +199,7 @@ def test_group16_runs_on_cuda_core_kernel():
     q = c.queries()
     ref = c.oracle_decode(q)
     for chunk in (0, 64):
-        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), ref) <= TOL
+        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), ref, floor=floor_for(c.w)) <= TOL
 
 
 @pytest.mark.parametrize("chunk", [0, 64])
@@ -206,7 +210,7 @@ def test_wide_query_groups_match_oracle(heads, chunk):
     w = wl.workload("llama8b", batch=2, n_heads=heads[0], n_kv_heads=heads[1])
     c = Case(w, [700, 33])
     q = c.queries()
-    assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q)) <= TOL
+    assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q), floor=floor_for(c.w)) <= TOL
     assert c.cache.status_bits() == 0
 
 
@@ -223,7 +227,7 @@ def test_several_v_groups_match_oracle(kv, heads, chunk):
                     k_group=g, v_group=g, k_param=par, v_param=par)
     c = Case(w, [1500, 41])
     q = c.queries()
-    assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q)) <= TOL
+    assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q), floor=floor_for(c.w)) <= TOL
     assert c.cache.status_bits() == 0
 
 
@@ -234,7 +238,7 @@ def test_several_v_groups_window_matches_oracle():
     q = c.queries()
     ref = c.oracle_decode(q, window=1000)
     for chunk in (0, 64):
-        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk, window=1000), ref) <= TOL
+        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk, window=1000), ref, floor=floor_for(c.w)) <= TOL
 
 
 def test_wide_query_group_affine_matches_oracle():
@@ -243,7 +247,7 @@ def test_wide_query_group_affine_matches_oracle():
     c = Case(w, [900, 17])
     q = c.queries()
     for chunk in (0, 64):
-        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q)) <= TOL
+        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), c.oracle_decode(q), floor=floor_for(c.w)) <= TOL
 
 
 def _tie_rows(w: dict, n_rows: int, seed: int) -> np.ndarray:
@@ -369,7 +373,7 @@ def test_bf16_activations_match_oracle(name):
     q = c.queries()
     ref = c.oracle_decode(q)
     for chunk in (0, 64):
-        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), ref) <= TOL_BF16_OUT, chunk
+        assert max_row_err(c.gpu_decode(q, chunk_tokens=chunk), ref, floor=floor_for(c.w)) <= TOL_BF16_OUT, chunk
     # the fused step: new rows at L - 1
     dev = c.cache.device
     k_new = _round_bf16(wl.new_rows(c._draws(), "k", c.B, step=1))
@@ -388,4 +392,4 @@ def test_bf16_activations_match_oracle(name):
     k, v = c.gpu_pools()
     assert np.array_equal(k, c.pools["k"]) and np.array_equal(v, c.pools["v"])
     got = out.float().cpu().numpy().astype(np.float64)
-    assert max_row_err(got, c.oracle_decode(q1)) <= TOL_BF16_OUT
+    assert max_row_err(got, c.oracle_decode(q1), floor=floor_for(c.w)) <= TOL_BF16_OUT
