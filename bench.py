@@ -1,17 +1,26 @@
 #!/usr/bin/env python
 """Decode-step benchmark of the quantized paged KV path on GB300.
 
-One step = one decode step through every layer of the workload's model.  Each
-layer runs kvq_append (quantize the new token's K/V row into its page) and
-kvq_decode_attention (or kvq_window_decode) over the layer's whole cache.  The
-layers' caches together are larger than L2, so each layer's KV comes from HBM
-on every step.  The step is captured once in a CUDA graph and replayed.
+One step = one decode step through every layer of a workload's model.  Each
+layer appends the new token's K/V row (quantized into its page) and runs the
+decode attention over the layer's whole cache, in one fused call
+(kvq_append_decode_attention, or kvq_append_window_decode for a sliding-window
+layer).  The step is captured once in a CUDA graph and replayed.
+
+The headline workload (default: the continuous batch, the largest single-GPU
+configuration) is timed, and so is every other configuration in `per_config`:
+the Llama-3.1-8B-shaped model, the sliding-window and the global layers of the
+sliding + global mix (separately and together) and the long mixed-dtype
+context.  Each is timed in blocks of exactly K steps, each block bracketed by a
+barrier and a device synchronize, and reports the median block.  A model whose
+caches together are smaller than twice the L2 cache gets an L2 flush before
+every timed step instead.
 
 Printed (rank 0, one JSON line): decode-attention KV GB/s for the whole job
 (algorithmic bytes / step time), query and context tokens/s, the roofline of
-the decode call (its average duration from CUDA events recorded inside the
-graph), the end-to-end number through host buffers, clocks seen during the
-timed region, and the CPU oracle timed on a bounded sample of the same work.
+the fused call, the end-to-end number through host buffers, clocks seen during
+the timed region, per-configuration results, and the CPU oracle timed on a
+bounded sample of the same work.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...      # the CPU oracle as the reference arm
@@ -38,13 +47,16 @@ import kvq_workloads as wl  # noqa: E402
 
 METRIC = "decode-attention KV GB/s and % of HBM peak; attention tokens/s at 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
 
 # Layers of each model: (workload, number of layers, window decode?)
 MODELS = {
-    "llama8b": [("llama8b", 32, False)],                       # Llama-3.1-8B: 32 layers
     "contbatch": [("contbatch", 1, False)],                    # 1.16 GB per layer already > L2
-    "long_mixed": [("long_mixed", 4, False)],
+    "llama8b": [("llama8b", 32, False)],                       # Llama-3.1-8B: 32 layers
     "gemma_mix": [("gemma_mix", 25, True), ("gemma_mix", 5, False)],   # 25 window + 5 global
+    "gemma_window": [("gemma_mix", 25, True)],                 # the window layers of gemma_mix
+    "gemma_global": [("gemma_mix", 5, False)],                 # the global layers of gemma_mix
+    "long_mixed": [("long_mixed", 4, False)],
     # the unquantised f16 K/V the pages compare with (8K and 64K)
     "llama8b_f16": [("llama8b_f16", 32, False)],
     "long_f16": [("long_f16", 4, False)],
@@ -52,9 +64,21 @@ MODELS = {
     "llama8b_shimmy": [("llama8b_shimmy", 32, False)],
     "long_shimmy": [("long_shimmy", 4, False)],
 }
+# Configurations timed besides the headline one.
+PER_CONFIG = ("contbatch", "llama8b", "gemma_window", "gemma_global", "gemma_mix", "long_mixed")
 
 
 # ----------------------------------------------------------------------------- helpers
+
+
+def kv_bytes_per_token_head(kind: str, head_dim: int, group: int, param: str) -> int:
+    """Stored bytes of one token's K or V vector for one kv head: codes plus the
+    scale (and bias) of every group; f16 rows have no scale."""
+    if kind == "f16":
+        return 2 * head_dim
+    bits = 8 if kind == "sym8" else 4
+    n_par = 2 if kind == "affine4" else 1
+    return head_dim * bits // 8 + (head_dim // group) * n_par * (4 if param == "f32" else 2)
 
 
 def algorithmic_bytes(w: dict, lens: np.ndarray, window: int) -> tuple[int, int]:
@@ -62,13 +86,12 @@ def algorithmic_bytes(w: dict, lens: np.ndarray, window: int) -> tuple[int, int]
 
     Decode: K/V codes and scales of every attended token, q, out, the block-table
     entries it reads and seq_lens.  Append: the new K/V rows, the RoPE row,
-    positions, and the codes and scales written.  Per-token sizes come from the
-    library's kvq_cache_bytes.
+    positions, and the codes and scales written.
     """
-    from int8_quantized_paged_gb300 import kvq
     hd, hkv, hq = w["head_dim"], w["n_kv_heads"], w["n_heads"]
     act = 4 if w["act"] == "f32" else 2
-    per_tok = kvq.cache_bytes(kvq.config(**w), 1, 16) // (16 * hkv)     # K + V bytes per token-head
+    per_tok = (kv_bytes_per_token_head(w["k_kind"], hd, w["k_group"], w["k_param"])
+               + kv_bytes_per_token_head(w["v_kind"], hd, w["v_group"], w["v_param"]))
     att = np.minimum(lens, window) if window else lens
     B = len(lens)
     dec = int(att.sum()) * hkv * per_tok + 2 * B * hq * hd * act + 4 * int(np.ceil(att / 16).sum()) + 4 * B
@@ -112,6 +135,25 @@ def load_peaks() -> tuple[float, str]:
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or 'unknown'."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 class _Cu:
@@ -235,6 +277,22 @@ def whole_job(units_per_rank: float, world: int, ms_max: float) -> float:
     return units_per_rank * world / (ms_max / 1e3)
 
 
+def n_blocks_for(block_ms: float, min_blocks: int = 5, min_seconds: float = 1.0, max_blocks: int = 400) -> int:
+    """How many timed blocks of block_ms each: at least min_blocks, and enough
+    for about min_seconds of timed work (so the clock sampler sees the load),
+    at most max_blocks."""
+    want = math.ceil(min_seconds * 1e3 / max(block_ms, 1e-6))
+    return int(min(max_blocks, max(min_blocks, want)))
+
+
+def check_gpus_flag(gpus: int, world: int) -> str | None:
+    """An error message when --gpus disagrees with the launch (WORLD_SIZE)."""
+    if gpus != world:
+        return (f"--gpus {gpus} but WORLD_SIZE is {world}: launch N ranks with "
+                f"torch.distributed.run --nproc-per-node N bench.py --gpus N")
+    return None
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 
@@ -330,15 +388,15 @@ class BenchLayer:
         return 1 + kvq.decode_launches(self.cache.cfg)
 
 
-def build_layers(args, dev, seed: int) -> list:
-    """The layers of args.workload's model, caches prefilled on the device."""
+def build_layers(model: str, args, dev, seed: int) -> list:
+    """The layers of a model, caches prefilled on the device."""
     import torch
     from int8_quantized_paged_gb300 import kvq
     layers = []
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
     rope_tabs = {}   # one RoPE table per model: every layer reads the same positions
-    for name, n, window in MODELS[args.workload]:
+    for name, n, window in MODELS[model]:
         w = wl.workload(name, **({"batch": args.batch} if args.batch else {}))
         if name not in rope_tabs:
             cfg = kvq.config(**w)
@@ -396,7 +454,7 @@ def run_profile(args) -> None:
     dev = torch.device("cuda", 0)
     from int8_quantized_paged_gb300 import build as _build
     _build.build()
-    layers = build_layers(args, dev, 1000)
+    layers = build_layers(args.workload, args, dev, 1000)
     torch.cuda.synchronize()
     for _ in range(args.profile_decode):
         for L in layers:
@@ -405,6 +463,174 @@ def run_profile(args) -> None:
     assert all(L.cache.status_bits() == 0 for L in layers), "a kernel flagged a bad input"
     print(f"profile-decode: {args.workload}, {len(layers)} layers x {args.profile_decode} calls, "
           f"{layers[0].dec_bytes} algorithmic bytes per call", flush=True)
+
+
+def l2_bytes(dev) -> int:
+    import torch
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20))
+
+
+def time_blocks(run_step, steps: int, stream, world: int, n_blocks: int, flush=None) -> list[float]:
+    """ms per step of each of n_blocks blocks of exactly `steps` steps.  Every
+    block is bracketed by a barrier and a device synchronize.  Without `flush`
+    the block's steps run back to back between two events; with it, `flush`
+    (a write larger than L2) runs before every step, and the block's time is
+    the sum of its steps' own event intervals."""
+    import torch
+    out = []
+    for _ in range(n_blocks):
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            if flush is None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(steps):
+                    run_step()
+                e1.record(stream)
+            else:
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(steps)]
+                for a, b in evs:
+                    flush()
+                    a.record(stream)
+                    run_step()
+                    b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        if flush is None:
+            out.append(e0.elapsed_time(e1) / steps)
+        else:
+            out.append(sum(a.elapsed_time(b) for a, b in evs) / steps)
+    return out
+
+
+def measure_model(model: str, args, dev, world: int, rank: int, headline: bool, clocks=None) -> dict:
+    """Builds, times and frees one model.  Returns the numbers of one bench line
+    (for the headline: with the bracketed launch time and the end-to-end leg)."""
+    import torch
+    layers = build_layers(model, args, dev, 1000 + 97 * rank)
+    io_in, io_out = stage_io(layers, dev)
+    torch.cuda.synchronize()
+    for L in layers:
+        assert L.cache.status_bits() == 0, "prefill flagged a bad page or position"
+
+    step_bytes = sum(L.dec_bytes + L.app_bytes for L in layers)
+    kv_bytes = sum(L.dec_bytes for L in layers)
+    query_tokens = layers[0].B
+    ctx_tokens = sum(int((np.minimum(L.lens, L.window) if L.window else L.lens).sum()) for L in layers)
+    stream = torch.cuda.Stream(device=dev)
+    flush_buf = None
+    if kv_bytes < 2 * l2_bytes(dev):
+        flush_buf = torch.empty(2 * l2_bytes(dev) // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        for L in layers:
+            L.step()
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    g_a = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_a, stream=stream):
+        step()
+    launches_per_step = sum(L.launches() for L in layers)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_a.replay()
+    torch.cuda.synchronize()
+
+    flush = (lambda: flush_buf.zero_()) if flush_buf is not None else None
+    # one calibration block sizes the timed run (the same block count on every rank)
+    cal = time_blocks(g_a.replay, args.steps, stream, world, 1, flush)[0]
+    n_blocks = int(max_over_ranks(n_blocks_for(cal * args.steps, min_seconds=args.min_seconds), world))
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+    blocks = time_blocks(g_a.replay, args.steps, stream, world, n_blocks, flush)
+    ms = statistics.median(blocks)
+    ms_max = max_over_ranks(ms, world)
+    res = {"layers": len(layers), "batch": layers[0].B, "ctx": int(layers[0].lens.max()),
+           "kv_bytes_per_step": step_bytes, "ms_per_step": ms_max, "blocks": n_blocks,
+           "block_ms_per_step": {"median": round(ms, 5), "min": round(min(blocks), 5),
+                                 "max": round(max(blocks), 5)},
+           "l2": ("an L2 flush (a write of twice the L2 size) before every timed step: the caches "
+                  "together (%.1f MB) are smaller than twice L2" % (kv_bytes / 1e6)) if flush else
+                 ("inputs larger than L2: %d layer caches of %.1f MB each are read in turn"
+                  % (len(layers), statistics.mean(L.dec_bytes for L in layers) / 1e6)),
+           "step_bytes": step_bytes, "query_tokens": query_tokens, "ctx_tokens": ctx_tokens,
+           "launches_per_step": launches_per_step,
+           "fused": any(L.fused() for L in layers),
+           "one_kernel": all(L.fused() and L.launches() == 1 for L in layers),
+           "call_bytes": statistics.mean(L.dec_bytes + (L.app_bytes if L.fused() else 0) for L in layers),
+           "workloads": sorted({L.w["name"] for L in layers})}
+
+    if headline:
+        # decode-call durations: a second graph with external event records
+        # around every call, one step per replay
+        cu = _Cu()
+        evs = [(cu.event(), cu.event()) for _ in layers]
+        g_b = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_b, stream=stream):
+            for L, (e0, e1) in zip(layers, evs):
+                if not L.fused():
+                    L.append()
+                cu.record_external(e0, torch.cuda.current_stream().cuda_stream)
+                L.step() if L.fused() else L.decode()
+                cu.record_external(e1, torch.cuda.current_stream().cuda_stream)
+        dec_ms = []
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                if flush:
+                    flush()
+                g_b.replay()
+                stream.synchronize()
+                dec_ms.extend(cu.elapsed_ms(e0, e1) for e0, e1 in evs)
+        torch.cuda.synchronize()
+        res["bracketed_ms"] = statistics.mean(dec_ms)
+
+        # end to end: every layer's inputs from pinned host memory in one copy, the
+        # step (the public call per layer), every layer's outputs back in one copy
+        h_in = io_in.cpu().pin_memory()
+        h_out = io_out.cpu().pin_memory()
+
+        def e2e_step():
+            io_in.copy_(h_in, non_blocking=True)
+            g_a.replay()
+            h_out.copy_(io_out, non_blocking=True)
+            stream.synchronize()
+
+        e2e = time_blocks(e2e_step, args.steps, stream, world, 5, flush)
+        res["e2e_ms"] = max_over_ranks(statistics.median(e2e), world)
+        res["h2d"] = h_in.numel() * h_in.element_size()
+        res["d2h"] = h_out.numel() * h_out.element_size()
+    if clocks is not None:
+        res["clocks"] = clocks.stop()
+    for L in layers:
+        assert L.cache.status_bits() == 0, "a kernel flagged a bad page, position or length"
+    del layers, io_in, io_out, g_a, flush_buf
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def summarize(r: dict, world: int, peak: float) -> dict:
+    """value, fractions and rates of one measured model."""
+    ms = r["ms_per_step"]
+    launch_ms = ms / r["launches_per_step"] if r["one_kernel"] else r.get("bracketed_ms", float("nan"))
+    achieved = r["call_bytes"] / (launch_ms / 1e3) / 1e9
+    value = whole_job(r["step_bytes"], world, ms) / 1e9
+    return {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "frac": round(achieved / peak, 4), "avg_launch_us": round(launch_ms * 1e3, 3),
+        "tokens_per_s": round(whole_job(r["query_tokens"], world, ms), 1),
+        "context_tokens_per_s": round(whole_job(r["ctx_tokens"], world, ms), 1),
+        "layers": r["layers"], "batch": r["batch"], "ctx": r["ctx"], "kv_bytes_per_step": r["step_bytes"],
+        "blocks": r["blocks"], "block_ms_per_step": r["block_ms_per_step"], "l2": r["l2"],
+        "_achieved": achieved, "_launch_ms": launch_ms,
+    }
 
 
 def run_gpu(args) -> dict | None:
@@ -417,119 +643,24 @@ def run_gpu(args) -> dict | None:
     if rank == 0 or world == 1:
         _build.build()
     barrier(world)
-    from int8_quantized_paged_gb300 import kvq
 
-    layers = build_layers(args, dev, 1000 + 97 * rank)
-    io_in, io_out = stage_io(layers, dev)
-    torch.cuda.synchronize()
-    for L in layers:
-        assert L.cache.status_bits() == 0, "prefill flagged a bad page or position"
-
-    step_bytes = sum(L.dec_bytes + L.app_bytes for L in layers)
-    query_tokens = layers[0].B
-    ctx_tokens = sum(int((np.minimum(L.lens, L.window) if L.window else L.lens).sum()) for L in layers)
-
-    stream = torch.cuda.Stream(device=dev)
-    cu = _Cu()
-
-    def step():
-        for L in layers:
-            L.step()
-
-    # warm up outside capture, then capture the step (graph A) and the step with
-    # external event records around every decode call (graph B): the fused
-    # append + decode call, or the decode call after a separate append.
-    with torch.cuda.stream(stream):
-        step()
-    torch.cuda.synchronize()
-    g_a = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_a, stream=stream):
-        step()
-    evs = [(cu.event(), cu.event()) for _ in layers]
-    g_b = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_b, stream=stream):
-        for L, (e0, e1) in zip(layers, evs):
-            if not L.fused():
-                L.append()
-            cu.record_external(e0, torch.cuda.current_stream().cuda_stream)
-            L.step() if L.fused() else L.decode()
-            cu.record_external(e1, torch.cuda.current_stream().cuda_stream)
-    # per layer: one fused launch on the tensor-core path; else the append
-    # kernel plus the decode call's kernels
-    launches_per_step = sum(L.launches() for L in layers)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            g_a.replay()
-    torch.cuda.synchronize()
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(args.steps):
-            g_a.replay()
-        t1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    ms = t0.elapsed_time(t1) / args.steps
-
-    # decode-call durations: graph B, one step per replay
-    dec_ms = []
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            g_b.replay()
-            stream.synchronize()
-            dec_ms.extend(cu.elapsed_ms(e0, e1) for e0, e1 in evs)
-    torch.cuda.synchronize()
-
-    # end to end: every layer's inputs from pinned host memory in one copy, the
-    # step (the public call per layer), every layer's outputs back in one copy
-    h_in = io_in.cpu().pin_memory()
-    h_out = io_out.cpu().pin_memory()
-    h2d = h_in.numel() * h_in.element_size()
-    d2h = h_out.numel() * h_out.element_size()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            io_in.copy_(h_in, non_blocking=True)
-            g_a.replay()
-            h_out.copy_(io_out, non_blocking=True)
-            stream.synchronize()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    clk = clocks.stop()
-    for L in layers:
-        assert L.cache.status_bits() == 0, "a kernel flagged a bad page, position or length"
-
-    ms_max = max_over_ranks(ms, world)
-    e2e_max = max_over_ranks(e2e_ms, world)
-    # bytes of the timed call: the decode's, plus the append's when it is fused in
-    dec_bytes = statistics.mean(L.dec_bytes + (L.app_bytes if L.fused() else 0) for L in layers)
-    fused = any(L.fused() for L in layers)
-    # Launch duration.  When every layer's step is one launch of the kernel,
-    # the timed region holds nothing else: its time over the launches is the
-    # kernel's average duration back to back (each launch's start overlapping
-    # the one before it, as in the step).  Otherwise the calls bracketed by
-    # events in graph B, which also holds their launch latency.
-    one_kernel = all(L.fused() and L.launches() == 1 for L in layers)
-    bracketed = statistics.mean(dec_ms)
-    dec_avg = ms / launches_per_step if one_kernel else bracketed
     peak, peak_kind = load_peaks()
-    achieved = dec_bytes / (dec_avg / 1e3) / 1e9
-    value = whole_job(step_bytes, world, ms_max) / 1e9
+    clocks = ClockSampler(local)
+    head = measure_model(args.workload, args, dev, world, rank, True, clocks)
+    hs = summarize(head, world, peak)
+    per_config = {}
+    if not args.no_per_config:
+        for m in PER_CONFIG:
+            if m == args.workload:
+                continue
+            s = summarize(measure_model(m, args, dev, world, rank, False), world, peak)
+            s.pop("_achieved")
+            s.pop("_launch_ms")
+            per_config[m] = s
+    ms_max = head["ms_per_step"]
     res = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": hs["value"],
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -542,47 +673,52 @@ def run_gpu(args) -> dict | None:
         "data": "synthetic: seeded N(0,1) activations of the workload's shapes; no model weights",
         "config": {
             "workload": args.workload,
-            "layers": len(layers),
-            "batch": layers[0].B,
-            "ctx": int(layers[0].lens.max()),
-            "kv_bytes_per_step": step_bytes,
-            "l2": "inputs larger than L2: %d layer caches of %.1f MB each are read in turn"
-                  % (len(layers), dec_bytes / 1e6),
+            "layers": head["layers"],
+            "batch": head["batch"],
+            "ctx": head["ctx"],
+            "kv_bytes_per_step": head["step_bytes"],
+            "l2": head["l2"],
+            "timing": (f"{head['blocks']} blocks of exactly {args.steps} steps, each bracketed by a barrier and a "
+                       f"device synchronize; ms_per_step is the median block"),
+            "block_ms_per_step": head["block_ms_per_step"],
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "graph": "CUDA graph of one step",
             "chunk_tokens": args.chunk_tokens or "library default",
             "step_call": ("kvq_append_decode_attention (window layers: kvq_append_window_decode)"
-                          if fused else "kvq_append + kvq_decode_attention (window layers: kvq_window_decode)"),
+                          if head["fused"] else
+                          "kvq_append + kvq_decode_attention (window layers: kvq_window_decode)"),
         },
-        "tokens_per_s": round(whole_job(query_tokens, world, ms_max), 1),
-        "context_tokens_per_s": round(whole_job(ctx_tokens, world, ms_max), 1),
-        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "tokens_per_s": hs["tokens_per_s"],
+        "context_tokens_per_s": hs["context_tokens_per_s"],
+        "pct_of_hbm_peak": hs["pct_of_hbm_peak"],
+        "pct_of_nominal_hbm": hs["pct_of_nominal_hbm"],
         "roofline": {
             "bound": "hbm",
             "kernel": ("decode_tc_kernel (kvq_append_decode_attention: the step's append, split-K decode "
-                       "and the LSE combine in one launch)" if fused else
+                       "and the LSE combine in one launch)" if head["fused"] else
                        "decode_tc_kernel (kvq_decode_attention: split-K decode with the LSE combine fused)"),
-            "achieved": round(achieved, 1),
+            "achieved": round(hs["_achieved"], 1),
             "peak": peak,
             "peak_source": f"{peak_kind} hbm_gbs",
             "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
+            "frac": round(hs["_achieved"] / peak, 4),
             "traffic": profiled_traffic(args.workload),
-            "algorithmic_bytes_per_launch": int(dec_bytes),
-            "avg_launch_us": round(dec_avg * 1e3, 3),
-            "launch_us_from": ("timed region / launches (the step is only this kernel)" if one_kernel
+            "algorithmic_bytes_per_launch": int(head["call_bytes"]),
+            "avg_launch_us": round(hs["_launch_ms"] * 1e3, 3),
+            "launch_us_from": ("timed region / launches (the step is only this kernel)" if head["one_kernel"]
                                else "CUDA events around each call in a graph of the step"),
-            "bracketed_launch_us": round(bracketed * 1e3, 3),
+            "bracketed_launch_us": round(head["bracketed_ms"] * 1e3, 3),
         },
         "e2e": {
-            "value": round(whole_job(step_bytes, world, e2e_max) / 1e9, 2),
+            "value": round(whole_job(head["step_bytes"], world, head["e2e_ms"]) / 1e9, 2),
             "unit": "GB/s",
-            "ms_per_step": round(e2e_max, 5),
-            "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(head["e2e_ms"], 5),
+            "h2d_bytes_per_step": head["h2d"],
+            "d2h_bytes_per_step": head["d2h"],
         },
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
+        "gpu_launches": head["launches_per_step"] * args.steps * head["blocks"],
+        "clocks": head["clocks"],
+        "per_config": per_config,
     }
     return res if rank == 0 else None
 
@@ -627,6 +763,9 @@ def oracle_sample(workload: str):
     return step, dec + app, desc
 
 
+ORACLE_KIND = "oracle (numpy, 1 thread, OPENBLAS_NUM_THREADS=1)"
+
+
 def cpu_worker(workload: str, seconds: float, steps: int, warmup: int) -> dict:
     step, nbytes, desc = oracle_sample(workload)
     for _ in range(warmup):
@@ -638,7 +777,8 @@ def cpu_worker(workload: str, seconds: float, steps: int, warmup: int) -> dict:
         step()
         times.append(time.perf_counter() - t)
     mean = sum(times) / len(times)
-    return {"value": round(nbytes / mean / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(nbytes / mean / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": ORACLE_KIND,
+            "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
             "sample": f"{desc}; {len(times)} timed calls, {mean * 1e3:.1f} ms each",
             "ms_per_step": mean * 1e3}
 
@@ -677,8 +817,8 @@ def run_reference(args) -> None:
         "dtype": "f64 (codes in fp32)",
         "data": "synthetic: seeded N(0,1) activations of the workload's shapes; no model weights",
         "config": {"workload": args.workload, "sample": r["sample"]},
-        "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
-                         "sample": r["sample"]},
+        "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": r["cores"], "kind": r["kind"],
+                         "cpu_model": r["cpu_model"], "host_cpus": r["host_cpus"], "sample": r["sample"]},
         "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -690,11 +830,14 @@ def run_reference(args) -> None:
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    ap.add_argument("--workload", choices=list(MODELS), default="llama8b")
+    ap.add_argument("--workload", choices=list(MODELS), default="contbatch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="timed work per configuration, at least (whole blocks, at least 5)")
     ap.add_argument("--chunk-tokens", type=int, default=0,
                     help="tokens per split-K chunk (0: the library chooses)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -705,20 +848,26 @@ def main():
                     help="time kvq_append + kvq_decode_attention instead of the fused call")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
-    if args.profile_decode:
-        run_profile(args)
-        return
-    if args.warmup < 3 and not args.cpu_worker and args.impl == "kvq":
-        ap.error("--warmup must be >= 3")
-
     if args.cpu_worker:
         print(json.dumps(cpu_worker(args.workload, args.cpu_seconds, args.steps, args.warmup)))
+        return
+    rank, world, _ = dist_env()
+    err = check_gpus_flag(args.gpus, world)
+    if err:
+        print(f"bench.py: {err}", file=sys.stderr)
+        sys.exit(2)
+    if args.profile_decode:
+        run_profile(args)
         return
     if args.impl == "reference":
         run_reference(args)
         return
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+
     res = run_gpu(args)
-    rank, world, _ = dist_env()
     if res is not None:
         if world == 1 and not args.no_cpu_baseline:
             cb = run_cpu_worker_subprocess(args.workload, args.cpu_seconds)

@@ -54,3 +54,68 @@ def test_profiled_traffic_is_keyed_by_the_source_hash():
     assert bench.profiled_traffic("no_such_workload") is None
     t = bench.profiled_traffic("llama8b")
     assert t is None or (isinstance(t, int) and t > 0)
+
+
+def test_closed_form_bytes_match_the_library_and_the_oracle():
+    """The bench's per-token byte count (no library call) equals the oracle's
+    sizing and the library's kvq_cache_bytes for every bench workload."""
+    import kvq_workloads as wl
+    from int8_quantized_paged_gb300 import kvq
+    from oracle import kvq_oracle as O
+    for name in wl.WORKLOADS:
+        w = wl.workload(name)
+        hd, hkv = w["head_dim"], w["n_kv_heads"]
+        per = (bench.kv_bytes_per_token_head(w["k_kind"], hd, w["k_group"], w["k_param"])
+               + bench.kv_bytes_per_token_head(w["v_kind"], hd, w["v_group"], w["v_param"]))
+        for which in ("k", "v"):
+            kind, grp, par = w[which + "_kind"], w[which + "_group"], w[which + "_param"]
+            assert bench.kv_bytes_per_token_head(kind, hd, grp, par) == O.bytes_per_token_head(kind, hd, grp, par)
+        assert per * 16 * hkv == kvq.cache_bytes(kvq.config(**w), 1, 16), name
+
+
+def test_algorithmic_bytes_of_the_llama8b_layer():
+    import numpy as np
+    import kvq_workloads as wl
+    w = wl.workload("llama8b")
+    dec, app = bench.algorithmic_bytes(w, np.array([8192]), 0)
+    # 8192 tokens x 8 kv heads x (68 + 68) B, q and out (2 x 32 x 128 x 2 B),
+    # 512 block-table entries and one length
+    assert dec == 8192 * 8 * 136 + 2 * 32 * 128 * 2 + 4 * 512 + 4
+    assert app == 2 * 8 * 128 * 2 + 4 * 128 + 8 + 8 * 136
+
+
+def test_block_count_and_gpus_flag():
+    assert bench.n_blocks_for(1000.0) == 5            # long blocks: the minimum of 5
+    assert bench.n_blocks_for(5.0) == 200             # about a second of timed work
+    assert bench.n_blocks_for(0.001) == 400           # capped
+    assert bench.check_gpus_flag(1, 1) is None
+    assert "WORLD_SIZE" in bench.check_gpus_flag(8, 1)
+
+
+def test_gpus_flag_mismatch_exits_nonzero():
+    import subprocess
+    import sys
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--gpus", "2"],
+                       capture_output=True, text=True, env=env, timeout=120)
+    assert r.returncode == 2 and "--gpus 2" in r.stderr
+
+
+def test_oracle_sample_loads_no_product_library():
+    """The CPU arm (cpu_baseline, --impl reference) runs the oracle only: its
+    process imports no part of the package and maps no libkvq.so."""
+    import subprocess
+    import sys
+    code = ("import sys, bench\n"
+            "step, nbytes, desc = bench.oracle_sample('tiny_model')\n"
+            "step()\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "assert 'libkvq' not in maps, 'libkvq mapped'\n"
+            "assert not any(m.startswith('int8_quantized_paged_gb300') for m in sys.modules), 'package imported'\n"
+            "print(nbytes)\n")
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1")
+    pre = ("import bench; bench.MODELS['tiny_model'] = [('tiny', 1, False)]\n")
+    r = subprocess.run([sys.executable, "-c", pre + code], capture_output=True, text=True, env=env,
+                       cwd=bench.ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert int(r.stdout.split()[-1]) > 0
