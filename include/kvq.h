@@ -91,7 +91,6 @@ typedef enum kvq_status {
 #define KVQ_DEV_BAD_POS 2         /* a position past the block table or the RoPE table */
 #define KVQ_DEV_BAD_SEQ 4         /* a sequence id outside [0, n_seqs) */
 #define KVQ_DEV_BAD_LEN 8         /* a seq_len < 0 or past the block table's capacity */
-#define KVQ_DEV_TIMEOUT 16        /* a bounded wait on a copy gave up (should never happen) */
 
 typedef enum kvq_float { KVQ_F32 = 0, KVQ_F16 = 1, KVQ_BF16 = 2 } kvq_float;
 
@@ -363,9 +362,12 @@ kvq_status kvq_append_window_decode(const kvq_config* cfg, int32_t batch, const 
  * KVQ_NOALLOC_SCRATCH_BYTES array compiled into the library.  Every GPU that
  * loads the library holds that array until the process exits.  A decode whose
  * workspace (kvq_decode_workspace_bytes) is larger returns
- * KVQ_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress) with that device
- * current, so make that first call before any stream capture.  All calls share
+ * KVQ_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The first call in a CUDA
+ * context of a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current, and the address is kept
+ * for that context.  A device reset gives the device a new context, where the
+ * array may sit elsewhere, so the next call looks it up again.  Make the first
+ * call in each context before any stream capture.  All calls share
  * the one array: calls whose kernels overlap on the GPU (for example on two
  * streams at once) race.  The library neither allocates nor frees memory here.
  * The array starts zeroed when the library loads, and every completed call

@@ -14,12 +14,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // 2^x with the hardware approximation (relative error about 2^-22, results
 // below 2^-126 flushed to zero); used for softmax weights in base 2.
 __device__ __forceinline__ float ex2(float x) {

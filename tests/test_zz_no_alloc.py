@@ -1,22 +1,28 @@
-"""kvq_decode_attention_noalloc against kvq_decode_attention.
+"""kvq_decode_attention_noalloc against kvq_decode_attention and the oracle.
 
 The no-allocation entry point is for callers that cannot allocate device
 memory themselves.  Examples are a plugin running inside an engine that owns
 all of HBM through its own pool, and a latency-critical path where an
 allocation and the synchronization it may bring are not allowed.  Its split-K
 workspace is a fixed array inside the library, so the caller passes only
-inputs and outputs.  These tests call it through the C ABI twice in a row,
-with different queries and lengths, and check each result against the entry
-point that takes a caller workspace.  The second call shows that the shared
-scratch left by the first call does not leak into the next result.  An
-oversized request must be refused before any launch.
+inputs and outputs.
+
+These tests call it through the C ABI several times in a row.  With
+chunk_tokens = 64 every call takes the workspace mode, whose last-arriving CTA
+of each (sequence, kv head) combines the partials through arrival counters in
+that shared array; two such calls back to back, then a third with another
+batch, show that what one call leaves in the array does not reach the next
+result.  Each result must equal, bit for bit, the entry point that takes a
+caller workspace (the same kernel on the same inputs), and match the oracle
+within the parity tolerance.  An oversized request must be refused before
+any launch.
 """
 import numpy as np
 import pytest
 import torch
 
 import kvq_workloads as wl
-from gpu_cases import TOL, Case
+from gpu_cases import TOL, Case, floor_for, max_row_err
 from int8_quantized_paged_gb300 import kvq
 from oracle import kvq_oracle as O
 
@@ -29,36 +35,53 @@ def _cuda():
         pytest.skip("needs a CUDA GPU")
 
 
-def _both(c: Case, q: np.ndarray, lens, chunk: int = 0):
+def _both(c: Case, q: np.ndarray, lens, chunk: int = 0, batch: int = 0):
+    """(no-alloc output, workspace-entry output) for the first `batch`
+    sequences (all when 0)."""
     dev = c.cache.device
-    qt = torch.from_numpy(q).to(dev)
-    lt = torch.from_numpy(np.asarray(lens, np.int32)).to(dev)
+    B = batch or c.B
+    qt = torch.from_numpy(np.ascontiguousarray(q[:B])).to(dev)
+    lt = torch.from_numpy(np.asarray(lens, np.int32)[:B]).to(dev)
+    table = c.cache.block_table[:B]          # rows 0 .. B-1: a contiguous prefix of the table
     ref = torch.full_like(qt, float("nan"))
     got = torch.full_like(qt, float("nan"))
-    ws = c.cache.workspace(c.B, chunk)
-    c.cache.decode(qt, lt, ref, ws, chunk)
-    kvq.decode_attention_noalloc(c.cfg, qt, c.cache.k_pool, c.cache.v_pool, c.n_pages, c.cache.block_table,
-                                 c.max_pages, lt, c.cache.rope_tab, c.rope_max, got, c.cache.status, chunk)
+    ws = torch.zeros(kvq.decode_workspace_bytes(c.cfg, B, c.max_pages, chunk), dtype=torch.uint8, device=dev)
+    kvq.decode_attention(c.cfg, qt, c.cache.k_pool, c.cache.v_pool, c.n_pages, table, c.max_pages, lt,
+                         c.cache.rope_tab, c.rope_max, ref, ws, c.cache.status, chunk)
+    kvq.decode_attention_noalloc(c.cfg, qt, c.cache.k_pool, c.cache.v_pool, c.n_pages, table, c.max_pages, lt,
+                                 c.cache.rope_tab, c.rope_max, got, c.cache.status, chunk)
     torch.cuda.synchronize()
     return got.double().cpu().numpy(), ref.double().cpu().numpy()
 
 
-def test_noalloc_matches_workspace_entry_twice():
+def _oracle(c: Case, q: np.ndarray, lens, batch: int = 0):
+    B = batch or c.B
+    return O.decode(c.spec, q[:B], c.pools, c.bt[:B], np.asarray(lens, np.int32)[:B])
+
+
+def test_noalloc_counter_path_twice_then_another_batch():
     w = wl.workload("llama8b", batch=3)
-    c = Case(w, [1000, 37, 2049], fill_oracle=False)
-    for step, lens, chunk in ((0, [1000, 37, 2049], 0), (1, [999, 5, 1500], 64)):
-        got, ref = _both(c, c.queries(step=step), lens, chunk)
-        assert np.all(np.isfinite(got))
-        assert float(np.max(O.row_rel_error(got, ref))) <= TOL, step
+    c = Case(w, [1000, 37, 2049])
+    calls = ((0, [1000, 37, 2049], 0), (1, [999, 5, 1500], 0), (2, [640, 33, 2049], 2))
+    for step, lens, batch in calls:
+        q = c.queries(step=step)
+        got, ref = _both(c, q, lens, chunk=64, batch=batch)
+        assert np.all(np.isfinite(got)), step
+        assert np.array_equal(got, ref), step
+        assert max_row_err(got, _oracle(c, q, lens, batch), floor=floor_for(c.w)) <= TOL, step
     assert c.cache.status_bits() == 0
 
 
-def test_noalloc_other_codec():
+def test_noalloc_library_chunks_and_other_codec():
     w = wl.workload("long_mixed", batch=2)
-    c = Case(w, [3000, 333], fill_oracle=False)
+    c = Case(w, [3000, 333])
     for step in (0, 1):
-        got, ref = _both(c, c.queries(step=step), [3000 - 7 * step, 333])
-        assert float(np.max(O.row_rel_error(got, ref))) <= TOL
+        lens = [3000 - 7 * step, 333]
+        q = c.queries(step=step)
+        got, ref = _both(c, q, lens)
+        assert np.array_equal(got, ref), step
+        assert max_row_err(got, _oracle(c, q, lens), floor=floor_for(c.w)) <= TOL, step
+    assert c.cache.status_bits() == 0
 
 
 def test_noalloc_rejects_oversized_workspace():
