@@ -196,6 +196,11 @@ class Pool:
         h = _vp()
         _check(lib().kvq_pool_create(n_pages, C.byref(h)))
         self._h = h
+        # Handles of the live tables over this pool.  The cyclic garbage
+        # collector may finalize a pool before a table that uses it; the pool
+        # then destroys those tables first (their pages go back into it), and
+        # a table destroys itself only while its pool still lists it.
+        self._tables = set()
 
     @property
     def handle(self):
@@ -220,6 +225,9 @@ class Pool:
 
     def close(self) -> None:
         if self._h:
+            for t in list(self._tables):
+                lib().kvq_table_destroy(_vp(t))
+            self._tables.clear()
             lib().kvq_pool_destroy(self._h)
             self._h = _vp()
 
@@ -237,6 +245,7 @@ class Table:
         h = _vp()
         _check(lib().kvq_table_create(pool.handle, n_seqs, max_pages_per_seq, page_size, C.byref(h)))
         self._h, self.pool = h, pool
+        pool._tables.add(h.value)
         self.n_seqs, self.max_pages = n_seqs, max_pages_per_seq
 
     def reserve(self, seq: int, n_rows: int) -> None:
@@ -256,7 +265,9 @@ class Table:
 
     def close(self) -> None:
         if self._h:
-            lib().kvq_table_destroy(self._h)
+            if self._h.value in self.pool._tables:
+                self.pool._tables.discard(self._h.value)
+                lib().kvq_table_destroy(self._h)
             self._h = _vp()
 
     def __del__(self):

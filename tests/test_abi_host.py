@@ -239,3 +239,27 @@ def test_workspace_sizes():
     assert kvq.window_workspace_bytes(cfg, 1, 1024, 64) < kvq.decode_workspace_bytes(cfg, 1, 1024, 64)
     with pytest.raises(kvq.KvqError):
         kvq.decode_workspace_bytes(cfg, 1, 512, 20)
+
+
+def test_pool_finalized_before_its_table_is_safe():
+    """The cyclic garbage collector may finalize a pool before a table that
+    holds it; neither order may touch freed host memory."""
+    import gc
+    for first in ("pool", "table"):
+        pool = kvq.Pool(8)
+        table = kvq.Table(pool, 2, 4)
+        table.reserve(0, 40)
+        assert pool.num_free == 5
+        if first == "pool":
+            pool.close()              # destroys the table first, then the pool
+            table.close()             # a no-op now
+        else:
+            table.close()
+            assert pool.num_free == 8
+            pool.close()
+        cycle = [kvq.Pool(4)]
+        cycle.append(kvq.Table(cycle[0], 1, 4))
+        cycle[1].reserve(0, 16)
+        cycle.append(cycle)           # a reference cycle the collector has to break
+        del cycle
+        gc.collect()
