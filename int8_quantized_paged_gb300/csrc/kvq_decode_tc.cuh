@@ -86,8 +86,11 @@ constexpr int kMaxCluster = 16;           // CTAs per cluster (a non-portable si
 // every CTA of the cluster [kMaxCluster][G], then the partial o of this CTA's
 // slice of the G * hd outputs from every CTA [cluster][per].
 constexpr int kRecvMl = kMaxCluster * 8 * 8;
+// Outputs a cluster CTA combines: its slice of the G * hd outputs, a multiple
+// of 4 (the partials move four outputs a store).
+__host__ __device__ inline int tc_per(int G, int hd, int cluster) { return ((G * hd + cluster - 1) / cluster + 3) & ~3; }
 inline size_t tc_recv_bytes(int G, int hd, int cluster) {
-  return kRecvMl + ((size_t)G * hd + cluster) * sizeof(float);
+  return kRecvMl + (size_t)cluster * tc_per(G, hd, cluster) * sizeof(float);
 }
 constexpr float kQScale = 256.0f;   // q is held x 2^8 in fp16 (hi/lo)
 constexpr float kWScale = 128.0f;   // w is held x 2^7 (w <= 2^8 * 2^7 < 65504)
@@ -1072,11 +1075,15 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   // past its ring; no copies are pending).  First the warps' running maxima,
   // then each warp's partial (o, l) scaled by 2^(m_w - M) with M the CTA's
   // maximum (0 for a warp that saw no key), so the merge itself is a sum.
+  // Output d of head h is kept at d ^ sw(h) of its row: the low two bits are
+  // XORed with the lane's head index, so the 32 lanes of one store hit 32
+  // different banks; readers take aligned groups of four and undo the XOR.
   __syncthreads();
   float* ows = reinterpret_cast<float*>(smem);   // [NW][G][HD]
   float* mws = ows + NW * G * HD;                // [NW][G]
   float* lws = mws + NW * G;                     // [NW][G]
   float* Mh = lws + NW * G;                      // [G]
+  auto sw = [&](int h) { return MRG ? (h >> 1) & 3 : h & 3; };
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int h = MRG ? 2 * tig + nt : 4 * nt + tig;   // head of slot nt (valid when < G)
@@ -1141,8 +1148,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
           o0 = fmaf(oacc[t][nt][1], 1.0f / tc::kLoScale, oacc[t][nt][0]);
           o1 = fmaf(oacc[t][nt][3], 1.0f / tc::kLoScale, oacc[t][nt][2]);
         }
-        ows[(w * G + h) * HD + d0] = fw * fmaf(o0, sc, pbg);
-        ows[(w * G + h) * HD + d1] = fw * fmaf(o1, sc, pbg);
+        ows[(w * G + h) * HD + (d0 ^ sw(h))] = fw * fmaf(o0, sc, pbg);
+        ows[(w * G + h) * HD + (d1 ^ sw(h))] = fw * fmaf(o1, sc, pbg);
       }
       if (gid == 0) {
         lws[w * G + h] = fw * lt;
@@ -1154,10 +1161,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 
   const int64_t cidx = ((int64_t)b * a.n_kv_heads + kvh) * a.n_chunks + chunk;
   // cluster mode: the CTA's merged partial goes straight into the receive
-  // buffers of the CTAs that combine it: output i to CTA i / per, and every
-  // head's (M, l) to every CTA
+  // buffers of the CTAs that combine it: outputs [i, i + 4) to CTA i / per,
+  // and every head's (M, l) to every CTA
   const int ncl = CL ? A.cluster : 1;
-  const int per = (G * HD + ncl - 1) / ncl;   // outputs combined per CTA
+  const int per = tc_per(G, HD, ncl);   // outputs combined per CTA
   const uint32_t rml = tc::smem_u32(smem) + (uint32_t)A.recv_off;
   const uint32_t rbo = rml + kRecvMl;
   const int rank = CL ? (int)tc::cluster_rank() : 0;
@@ -1172,22 +1179,46 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       tc::st_cluster_f2(tc::cluster_addr(rml + 8 * (rank * G + h), c), Mh[h], ls);
     }
   }
-  for (int i = tid; i < G * HD; i += NW * 32) {
+  for (int i = 4 * tid; i < G * HD; i += 4 * NW * 32) {
     const int h = i / HD, d = i - h * HD;
     const float M = Mh[h];
-    float o = 0.f, ls = 0.f;
+    float o[4] = {0.f, 0.f, 0.f, 0.f}, ls = 0.f;
 #pragma unroll
     for (int w2 = 0; w2 < NW; ++w2) {
-      o += ows[(w2 * G + h) * HD + d];
+      const float4 x = *reinterpret_cast<const float4*>(ows + (w2 * G + h) * HD + d);
+      o[0] += x.x;
+      o[1] += x.y;
+      o[2] += x.z;
+      o[3] += x.w;
       ls += lws[w2 * G + h];
+    }
+    // stored position j holds output d + (j ^ sw(h)): undo the XOR by swaps
+    const int k = sw(h);
+    float r0 = o[0], r1 = o[1], r2 = o[2], r3 = o[3];
+    if (k & 1) {
+      const float t0 = r0, t2 = r2;
+      r0 = r1;
+      r1 = t0;
+      r2 = r3;
+      r3 = t2;
+    }
+    if (k & 2) {
+      const float t0 = r0, t1 = r1;
+      r0 = r2;
+      r1 = r3;
+      r2 = t0;
+      r3 = t1;
     }
     if constexpr (CL) {
       const int own = i / per;
-      tc::st_cluster_f(tc::cluster_addr(rbo + 4 * (rank * per + i - own * per), own), o);
+      tc::st_cluster_f4(tc::cluster_addr(rbo + 4 * (rank * per + i - own * per), own), r0, r1, r2, r3);
     } else if (nch == 1) {
-      store_act(A.out, a.act, obase + i, ls > 0.f ? o / ls : 0.f);
+      store_act(A.out, a.act, obase + i, ls > 0.f ? r0 / ls : 0.f);
+      store_act(A.out, a.act, obase + i + 1, ls > 0.f ? r1 / ls : 0.f);
+      store_act(A.out, a.act, obase + i + 2, ls > 0.f ? r2 / ls : 0.f);
+      store_act(A.out, a.act, obase + i + 3, ls > 0.f ? r3 / ls : 0.f);
     } else {
-      a.ws_acc[(cidx * G + h) * HD + d] = o;
+      *reinterpret_cast<float4*>(a.ws_acc + (cidx * G + h) * HD + d) = make_float4(r0, r1, r2, r3);
       if (d == 0) {
         a.ws_ml[(cidx * G + h) * 2] = M;
         a.ws_ml[(cidx * G + h) * 2 + 1] = ls;
