@@ -656,6 +656,7 @@ def run_gpu(args) -> dict | None:
             s = summarize(measure_model(m, args, dev, world, rank, False), world, peak)
             s.pop("_achieved")
             s.pop("_launch_ms")
+            s["traffic"] = profiled_traffic(m)   # DRAM bytes of one launch, when profiled
             per_config[m] = s
     ms_max = head["ms_per_step"]
     res = {
