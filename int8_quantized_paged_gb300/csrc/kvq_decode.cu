@@ -111,10 +111,10 @@ static TcLaunch tc_launcher(const kvq_config& c) {
   return table[kind][c.k_param_dtype];
 }
 
-// Bytes of one warp's ring of page slots.
-static size_t tc_ring_bytes(const kvq_config& c) {
+// Bytes of one warp's ring of page slots (the cluster mode keeps more pages in flight).
+static size_t tc_ring_bytes(const kvq_config& c, bool cluster) {
   const int G = c.n_heads / c.n_kv_heads;
-  return (size_t)tc_depth(c.head_dim, G > 4 ? 2 : 1, c.k_dtype) *
+  return (size_t)tc_depth(c.head_dim, G > 4 ? 2 : 1, c.k_dtype, cluster) *
          tc_slot_bytes(c.k_dtype, c.v_dtype, c.head_dim, tc_ng(c), c.k_param_dtype);
 }
 
@@ -350,7 +350,7 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     // Shared memory: a ring of tc_depth pages per warp and the query's
     // fragments, reused at the end for the warps' merge and then either the
     // cluster's partial or the combine's weights.
-    const size_t ring = tc_ring_bytes(*cfg);
+    const size_t ring_cl = tc_ring_bytes(*cfg, true), ring = tc_ring_bytes(*cfg, false);
     const size_t pre = tc_pre_bytes(hd, nt, ng);
     auto merge_bytes = [&](int warps) { return ((size_t)warps * G * (hd + 2) + G) * sizeof(float); };
     TcLaunchCfg lc{};
@@ -358,7 +358,7 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     lc.pdl = pdl_enabled();
 
     int cb = 0, recv = 0;
-    if (chunk_tokens == 0 && pick_cluster(*cfg, batch, max_tokens, window, fn, ring, pre, &lc, &cb, &recv)) {
+    if (chunk_tokens == 0 && pick_cluster(*cfg, batch, max_tokens, window, fn, ring_cl, pre, &lc, &cb, &recv)) {
       t.cluster = lc.cluster;
       t.blocks_per_chunk = cb;
       t.recv_off = recv;
@@ -443,7 +443,7 @@ extern "C" int32_t kvq_decode_cluster_ctas(const kvq_config* cfg, int32_t batch,
   const int64_t max_tokens = window > 0 ? window : (int64_t)max_pages_per_seq * cfg->page_size;
   TcLaunchCfg lc{};
   int cb = 0, recv = 0;
-  const bool on = pick_cluster(*cfg, batch, max_tokens, window, tc_launcher(*cfg), tc_ring_bytes(*cfg),
+  const bool on = pick_cluster(*cfg, batch, max_tokens, window, tc_launcher(*cfg), tc_ring_bytes(*cfg, true),
                                tc_pre_bytes(cfg->head_dim, G > 4 ? 2 : 1, tc_ng(*cfg)), &lc, &cb, &recv);
   return on ? lc.cluster : 0;
 }

@@ -98,9 +98,12 @@ constexpr float kLazyMax = 8.0f;    // raise the running max only past +2^8
 
 // Pages in flight per warp, and CTAs per SM (the launch bounds), by shape.
 // f16 K/V pages are 4 times larger: 2 in flight per warp at hd 128 (4 at hd 64),
-// 3 CTAs per SM.
-__host__ __device__ constexpr int tc_depth(int hd, int nt, int kind = KVQ_SYM_INT4) {
-  return kind == KVQ_F16_KV ? (hd == 128 ? 2 : 4) : ((hd == 256 || nt == 2) ? 3 : 4);
+// 3 CTAs per SM.  4-bit pages at head_dim <= 128 keep 4 in flight in the
+// cluster mode (one CTA per SM: 8 warps carry the whole page stream; measured
+// 9.4 against 8.6 us per llama8b layer with 3) and 3 in the workspace mode,
+// where 20 warps per SM do (continuous batch +0.9 % against 4).
+__host__ __device__ constexpr int tc_depth(int hd, int nt, int kind = KVQ_SYM_INT4, bool cl = false) {
+  return kind == KVQ_F16_KV ? (hd == 128 ? 2 : 4) : ((hd == 256 || nt == 2) ? 3 : (cl ? 4 : 3));
 }
 __host__ __device__ constexpr int tc_min_blocks(int hd, int nt, int kind = KVQ_SYM_INT4) {
   return kind == KVQ_F16_KV ? 3 : (hd <= 128 ? (nt == 1 ? 5 : 4) : 3);
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(32 * (CL ? kClusterWarps : kWarps),
 decode_tc_kernel(const __grid_constant__ TcArgs A) {
   constexpr int P = 16;
   constexpr int NW = CL ? kClusterWarps : kWarps;
-  constexpr int D = tc_depth(HD, NT, KK);       // pages in flight per warp
+  constexpr int D = tc_depth(HD, NT, KK, CL);   // pages in flight per warp
   constexpr bool K8 = KK == KVQ_SYM_INT8, V8 = VK == KVQ_SYM_INT8;
   constexpr bool KAFF = KK == KVQ_AFFINE_INT4, VAFF = VK == KVQ_AFFINE_INT4;
   // 4-bit conversion modes (kvq_tc_ptx.cuh): 0 symmetric, 1 affine, 2 offset-binary (shimmy4)
