@@ -4,6 +4,7 @@ end-to-end step), and the kernel-source hash that keys the profiled traffic."""
 import os
 from types import SimpleNamespace
 
+import pytest
 import torch
 
 import bench
@@ -119,3 +120,25 @@ def test_oracle_sample_loads_no_product_library():
                        cwd=bench.ROOT, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert int(r.stdout.split()[-1]) > 0
+
+
+def test_summarize_rates_and_fractions():
+    """One measured model's numbers: whole-job GB/s from the step bytes, the
+    launch time from the step (one kernel a layer) and the roofline fraction."""
+    r = {"ms_per_step": 0.25, "launches_per_step": 32, "one_kernel": True, "call_bytes": 8.0e6,
+         "step_bytes": 2.56e8, "query_tokens": 1, "ctx_tokens": 32 * 8192, "layers": 32, "batch": 1,
+         "ctx": 8192, "blocks": 7, "block_ms_per_step": {"median": 0.25}, "l2": "x"}
+    s = bench.summarize(r, 1, 6000.0)
+    assert s["value"] == pytest.approx(1024.0)                 # 2.56e8 B / 0.25 ms
+    assert s["avg_launch_us"] == pytest.approx(0.25e3 / 32, abs=1e-3)   # the step over its launches
+    assert s["frac"] == pytest.approx(8.0e6 / (0.25e-3 / 32) / 1e9 / 6000.0, rel=1e-3)
+    assert s["pct_of_hbm_peak"] == pytest.approx(100 * 1024.0 / 6000.0, abs=0.01)
+    assert s["pct_of_nominal_hbm"] == pytest.approx(100 * 1024.0 / 8000.0, abs=0.01)
+    assert s["tokens_per_s"] == pytest.approx(4000.0)
+    assert s["context_tokens_per_s"] == pytest.approx(32 * 8192 / 0.25e-3)
+    # two replicas: the job's value counts both ranks' bytes over the slowest rank's time
+    s2 = bench.summarize(r, 2, 6000.0)
+    assert s2["value"] == pytest.approx(2048.0) and s2["pct_of_hbm_peak"] == s["pct_of_hbm_peak"]
+    # with more than one launch a layer, the launch time is the bracketed one
+    r3 = dict(r, one_kernel=False, bracketed_ms=0.01)
+    assert bench.summarize(r3, 1, 6000.0)["avg_launch_us"] == pytest.approx(10.0)
