@@ -298,7 +298,7 @@ def check_gpus_flag(gpus: int, world: int) -> str | None:
 
 class BenchLayer:
     def __init__(self, w: dict, window: bool, layer: int, device, gen, chunk_tokens: int = 0,
-                 rope_tab=None):
+                 rope_tab=None, flags: int = 0):
         import torch
         from int8_quantized_paged_gb300 import kvq
         from int8_quantized_paged_gb300.cache import LayerCache
@@ -307,7 +307,7 @@ class BenchLayer:
         self.B = len(self.lens)
         self.window = int(w["window"]) if window else 0
         self.ring = int(w["ring_rows"]) if window else 0
-        cfg = kvq.config(**w)
+        cfg = kvq.config(**w, flags=flags)
         P = 16
         if self.ring:
             max_pages = self.ring // P
@@ -388,6 +388,15 @@ class BenchLayer:
         return 1 + kvq.decode_launches(self.cache.cfg)
 
 
+def early_reads(model: str, args) -> bool:
+    """Whether a model's calls may read their pages before the kernel before
+    them ends (KVQ_FLAG_EARLY_READS).  That kernel must write none of those
+    inputs: true when it is another layer's fused call, not when a one-layer
+    model's call follows its own previous step or a separate append."""
+    n_layers = sum(n for _, n, _ in MODELS[model])
+    return n_layers > 1 and not args.separate and not getattr(args, "no_early_reads", False)
+
+
 def build_layers(model: str, args, dev, seed: int) -> list:
     """The layers of a model, caches prefilled on the device."""
     import torch
@@ -395,6 +404,7 @@ def build_layers(model: str, args, dev, seed: int) -> list:
     layers = []
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
+    flags = kvq.FLAG_EARLY_READS if early_reads(model, args) else 0
     rope_tabs = {}   # one RoPE table per model: every layer reads the same positions
     for name, n, window in MODELS[model]:
         w = wl.workload(name, **({"batch": args.batch} if args.batch else {}))
@@ -404,7 +414,7 @@ def build_layers(model: str, args, dev, seed: int) -> list:
             rope_tabs[name] = (torch.from_numpy(kvq.rope_table(cfg, rows)).to(dev)
                                if cfg.rope != kvq.ROPE_NONE else None)
         for i in range(n):
-            layers.append(BenchLayer(w, window, len(layers), dev, gen, args.chunk_tokens, rope_tabs[name]))
+            layers.append(BenchLayer(w, window, len(layers), dev, gen, args.chunk_tokens, rope_tabs[name], flags))
     # One decode step has one seq_lens and one positions array for all layers
     # of a model, as the model's layers share them; q and the new K/V rows
     # stay per layer.
@@ -561,6 +571,7 @@ def measure_model(model: str, args, dev, world: int, rank: int, headline: bool, 
            "step_bytes": step_bytes, "query_tokens": query_tokens, "ctx_tokens": ctx_tokens,
            "launches_per_step": launches_per_step,
            "fused": any(L.fused() for L in layers),
+           "early_reads": bool(layers[0].cache.cfg.flags & 1),
            "one_kernel": all(L.fused() and L.launches() == 1 for L in layers),
            "call_bytes": statistics.mean(L.dec_bytes + (L.app_bytes if L.fused() else 0) for L in layers),
            "workloads": sorted({L.w["name"] for L in layers})}
@@ -629,6 +640,7 @@ def summarize(r: dict, world: int, peak: float) -> dict:
         "context_tokens_per_s": round(whole_job(r["ctx_tokens"], world, ms), 1),
         "layers": r["layers"], "batch": r["batch"], "ctx": r["ctx"], "kv_bytes_per_step": r["step_bytes"],
         "blocks": r["blocks"], "block_ms_per_step": r["block_ms_per_step"], "l2": r["l2"],
+        "early_reads": r.get("early_reads", False),
         "_achieved": achieved, "_launch_ms": launch_ms,
     }
 
@@ -845,6 +857,8 @@ def main():
     ap.add_argument("--profile-decode", type=int, default=0, metavar="CALLS",
                     help="only run CALLS decode calls per layer (for profiler captures)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
+    ap.add_argument("--no-early-reads", action="store_true",
+                    help="multi-layer models: read every input after the previous kernel ends")
     ap.add_argument("--separate", action="store_true",
                     help="time kvq_append + kvq_decode_attention instead of the fused call")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)

@@ -129,9 +129,33 @@ typedef struct kvq_config {
   int32_t act_dtype;      /* kvq_float of q, k_new, v_new and out */
   int32_t rope;           /* kvq_rope */
   float attn_scale;       /* > 0: the score scale; <= 0: 1/sqrt(head_dim) */
-  int32_t reserved;       /* must be 0 */
+  int32_t flags;          /* 0, or KVQ_FLAG_EARLY_READS; other bits are INVALID_ARG */
   double rope_base;       /* theta_i = rope_base^(-2i/head_dim) */
 } kvq_config;
+
+/* kvq_config.flags.
+ *
+ * KVQ_FLAG_EARLY_READS: a decode call (kvq_decode_attention, its no-alloc and
+ * window forms, and the two fused append + decode calls) may read seq_lens,
+ * pos, the block table, the RoPE table and the pool pages before the kernel
+ * launched just before it on the same stream has finished.  The library
+ * launches its kernels with programmatic dependent launch, so a call can start
+ * while that kernel still runs; with the flag it streams its first pages in
+ * that time.  q, k_new and v_new are read only after that kernel has
+ * finished, and the output, the workspace and the new rows are written only
+ * after it; a bad input found earlier is flagged in dev_status, an atomic OR.
+ * The flag is a permission: a call may also read everything after the wait.
+ *
+ * Set it only when the kernel launched just before each call writes none of
+ * the inputs read early.  That holds in a multi-layer decode loop, where the
+ * kernel before a layer's call is the previous layer's call (other pools) or
+ * the projection that makes q, k_new and v_new.  It does not hold for
+ * back-to-back calls on the same pools, such as a single-layer model's
+ * consecutive steps, or a kvq_decode_attention right after the kvq_append that
+ * wrote its new row.  A copy (cudaMemcpyAsync) is not a kernel: the call
+ * starts after it completes.  Only the kernel immediately before can overlap:
+ * a call triggers the launch of the next one only after its own wait. */
+#define KVQ_FLAG_EARLY_READS 1
 
 /* ABI version of the loaded library (KVQ_ABI_VERSION). */
 int32_t kvq_abi_version(void);

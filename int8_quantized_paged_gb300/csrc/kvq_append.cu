@@ -40,7 +40,8 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendArgs a) {
   const int lane = threadIdx.x & 31;
   // Programmatic dependent launch: the new rows may come from the kernel
   // before this one; the kernel after it may start launching at once (it
-  // waits for this grid before reading the pools).
+  // waits for this grid before reading the pools: a decode with early reads
+  // is not to follow an append to its own pools).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;

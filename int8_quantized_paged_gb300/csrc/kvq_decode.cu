@@ -340,6 +340,7 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     t.vp_bytes = cfg->page_size * a.vl.param_row_bytes;
     t.cluster = 0;
     t.recv_off = 0;
+    t.early = (cfg->flags & KVQ_FLAG_EARLY_READS) != 0;
     const int nt = G > 4 ? 2 : 1;
     const int hd = cfg->head_dim;
     const int ng = tc_ng(*cfg);   // scale groups per head (K and V alike)

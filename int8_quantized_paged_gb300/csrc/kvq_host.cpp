@@ -44,7 +44,7 @@ static kvq_status check_common(const kvq_config* c) {
   if (c->head_dim < 2 || c->head_dim % 2 != 0)
     return fail(KVQ_ERR_INVALID_ARG, "head_dim (%d) must be a positive even number", c->head_dim);
   if (c->page_size < 1) return fail(KVQ_ERR_INVALID_ARG, "page_size (%d) must be >= 1", c->page_size);
-  if (c->reserved != 0) return fail(KVQ_ERR_INVALID_ARG, "reserved must be 0");
+  if (c->flags & ~KVQ_FLAG_EARLY_READS) return fail(KVQ_ERR_INVALID_ARG, "unknown flags 0x%x", c->flags);
   const int32_t kinds[2] = {c->k_dtype, c->v_dtype};
   const int32_t groups[2] = {c->k_group, c->v_group};
   const int32_t params[2] = {c->k_param_dtype, c->v_param_dtype};

@@ -23,6 +23,7 @@ DEV_BAD_PAGE, DEV_BAD_POS, DEV_BAD_SEQ, DEV_BAD_LEN = 1, 2, 4, 8
 F32, F16, BF16 = 0, 1, 2
 SYM_INT4, SYM_INT8, AFFINE_INT4, F16_KV, F32_KV, SHIMMY_INT4 = range(6)
 ROPE_NONE, ROPE_NORMAL, ROPE_NEOX = 0, 1, 2
+FLAG_EARLY_READS = 1
 
 FLOATS = {"f32": F32, "f16": F16, "bf16": BF16}
 KINDS = {"sym4": SYM_INT4, "sym8": SYM_INT8, "affine4": AFFINE_INT4, "f16": F16_KV, "f32": F32_KV,
@@ -42,16 +43,16 @@ class Config(C.Structure):
                 ("page_size", C.c_int32), ("k_dtype", C.c_int32), ("v_dtype", C.c_int32),
                 ("k_group", C.c_int32), ("v_group", C.c_int32), ("k_param_dtype", C.c_int32),
                 ("v_param_dtype", C.c_int32), ("act_dtype", C.c_int32), ("rope", C.c_int32),
-                ("attn_scale", C.c_float), ("reserved", C.c_int32), ("rope_base", C.c_double)]
+                ("attn_scale", C.c_float), ("flags", C.c_int32), ("rope_base", C.c_double)]
 
 
 def config(n_heads, n_kv_heads, head_dim, page_size=16, k_kind="sym4", v_kind="sym4",
            k_group=128, v_group=128, k_param="f32", v_param="f32", act="f16",
-           attn_scale=0.0, rope="normal", rope_base=10000.0, **_ignored) -> Config:
+           attn_scale=0.0, rope="normal", rope_base=10000.0, flags=0, **_ignored) -> Config:
     """A kvq_config from the names used in workload descriptions."""
     return Config(n_heads, n_kv_heads, head_dim, page_size, KINDS[k_kind], KINDS[v_kind],
                   k_group, v_group, FLOATS[k_param], FLOATS[v_param], FLOATS[act],
-                  ROPES[rope], float(attn_scale), 0, float(rope_base))
+                  ROPES[rope], float(attn_scale), int(flags), float(rope_base))
 
 
 _lib = None

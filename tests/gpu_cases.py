@@ -30,7 +30,7 @@ class Case:
     """A workload with explicit sequence lengths, filled on both sides."""
 
     def __init__(self, w: dict, lens, ring_rows: int = 0, shuffle: bool = True, extra_pages: int = 3,
-                 oracle_seqs=None, fill_oracle: bool = True):
+                 oracle_seqs=None, fill_oracle: bool = True, extra_positions: int = 0):
         self.w = w
         self.lens = np.asarray(lens, dtype=np.int32)
         self.B = len(self.lens)
@@ -48,7 +48,7 @@ class Case:
         if shuffle:
             pool.alloc(self.n_pages)
             pool.free(wl.page_free_order(w, self.n_pages))
-        self.rope_max = max(2, int(self.lens.max()) + 1)
+        self.rope_max = max(2, int(self.lens.max()) + 1 + extra_positions)
         self.cache = LayerCache(self.cfg, self.B, self.max_pages, self.n_pages, self.rope_max, ring_rows,
                                 pool=pool)
         for b, L in enumerate(self.lens):

@@ -122,9 +122,11 @@ def test_validate_config():
             kvq.validate_config(_cfg(w))
         assert e.value.status == want, over
     c = _cfg(wl.workload("llama8b"))
-    c.reserved = 1
+    c.flags = kvq.FLAG_EARLY_READS
+    kvq.validate_config(c)                            # the one defined flag
+    c.flags = 2
     with pytest.raises(kvq.KvqError):
-        kvq.validate_config(c)
+        kvq.validate_config(c)                        # an unknown bit
 
 
 def test_pool_lifo_and_errors():

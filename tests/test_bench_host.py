@@ -142,3 +142,15 @@ def test_summarize_rates_and_fractions():
     # with more than one launch a layer, the launch time is the bracketed one
     r3 = dict(r, one_kernel=False, bracketed_ms=0.01)
     assert bench.summarize(r3, 1, 6000.0)["avg_launch_us"] == pytest.approx(10.0)
+
+
+def test_early_reads_only_where_the_previous_kernel_is_another_layer():
+    """KVQ_FLAG_EARLY_READS lets a call read its pages before the kernel before
+    it ends, so the bench sets it only for models of several layers, each call
+    following another layer's, and never for the separate append + decode."""
+    a = SimpleNamespace(separate=False, no_early_reads=False)
+    assert bench.early_reads("llama8b", a) and bench.early_reads("gemma_window", a)
+    assert bench.early_reads("long_mixed", a)
+    assert not bench.early_reads("contbatch", a)            # one layer: its own previous step
+    assert not bench.early_reads("llama8b", SimpleNamespace(separate=True, no_early_reads=False))
+    assert not bench.early_reads("llama8b", SimpleNamespace(separate=False, no_early_reads=True))
