@@ -568,6 +568,16 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
                        : "memory");
     }
   };
+  // Cluster mode at head_dim 256, whole context, early reads: the pages wait
+  // for warp 0's q and RoPE requests, which would otherwise queue behind the
+  // prologue's page burst (3 pages of 4.6 KB a warp on 96 SMs, about 1.6 us
+  // of HBM time).  The cluster's CTAs do not start before the previous
+  // kernel ends (its clusters hold the SMs), so holding the pages back costs
+  // no overlap.  Measured per global layer 24.7 -> 24.0-24.3 us; at head_dim 128
+  // (a 6.7 MB burst) the same barrier cost llama8b 8.29 -> 8.55 us.
+  if constexpr (CL && EARLY && HD == 256) {
+    if (whole) __syncthreads();
+  }
 #pragma unroll
   for (int k = 0; k < D; ++k) {
     if (k < n_local) issue(k, k);
