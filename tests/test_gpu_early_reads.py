@@ -41,6 +41,9 @@ CASES = {
     "llama8b_b3": dict(name="llama8b", lens=[1000, 33, 2049], over=dict(batch=3), chain_kv=False),
     "long_mixed": dict(name="long_mixed", lens=[5000, 777], over=dict(batch=2), chain_kv=False),
     "gemma_window": dict(name="gemma_mix", lens=[3001], ring=1152, window=1024, chain_kv=True),
+    # head_dim 256, whole context: the cluster CTAs hold their page copies at a
+    # block barrier until warp 0 has issued its q and RoPE requests
+    "gemma_global": dict(name="gemma_mix", lens=[3001], chain_kv=True),
 }
 
 
@@ -118,6 +121,7 @@ DECODE_CASES = {
     # shares the library's one scratch workspace with the call before it
     "llama8b_noalloc": dict(name="llama8b", lens=[1000, 33, 2049], over=dict(batch=3)),
     "gemma_window": dict(name="gemma_mix", lens=[3001, 700], over=dict(batch=2), ring=1152, window=1024),
+    "gemma_global": dict(name="gemma_mix", lens=[3001, 700], over=dict(batch=2)),
 }
 
 
