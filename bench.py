@@ -515,6 +515,51 @@ def time_blocks(run_step, steps: int, stream, world: int, n_blocks: int, flush=N
     return out
 
 
+def time_pipelined(graphs, ins, outs, h_in, h_out, stream, steps: int, world: int, n_blocks: int) -> list[float]:
+    """ms per step of n_blocks blocks of `steps` end-to-end steps, pipelined over
+    two buffer sets: step i uploads its inputs into set i % 2 on a copy stream
+    (once the step that last read that set has run), the compute stream replays
+    that set's graph, and a second copy stream brings its outputs back.  So the
+    upload of step i+1 and the download of step i-1 overlap the compute of step
+    i.  Each block's time runs from before its first upload to after its last
+    download."""
+    import torch
+    up, down = torch.cuda.Stream(device=stream.device), torch.cuda.Stream(device=stream.device)
+    out = []
+    for _ in range(n_blocks):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        drained = [torch.cuda.Event() for _ in range(2)]
+        e0.record(stream)
+        up.wait_stream(stream)
+        for i in range(steps):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(done[b])            # step i-2 has read set b's inputs
+                ins[b].copy_(h_in, non_blocking=True)
+                ready[b].record(up)
+            stream.wait_event(ready[b])
+            if i >= 2:
+                stream.wait_event(drained[b])         # step i-2's outputs are back on the host
+            with torch.cuda.stream(stream):
+                graphs[b].replay()
+            done[b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(done[b])
+                h_out.copy_(outs[b], non_blocking=True)
+                drained[b].record(down)
+        stream.wait_stream(down)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        out.append(e0.elapsed_time(e1) / steps)
+    return out
+
+
 def measure_model(model: str, args, dev, world: int, rank: int, headline: bool, clocks=None) -> dict:
     """Builds, times and frees one model.  Returns the numbers of one bench line
     (for the headline: with the bracketed launch time and the end-to-end leg)."""
@@ -612,9 +657,26 @@ def measure_model(model: str, args, dev, world: int, rank: int, headline: bool, 
             stream.synchronize()
 
         e2e = time_blocks(e2e_step, args.steps, stream, world, 5, flush)
-        res["e2e_ms"] = max_over_ranks(statistics.median(e2e), world)
+        res["e2e_serial_ms"] = max_over_ranks(statistics.median(e2e), world)
+        res["e2e_ms"] = res["e2e_serial_ms"]
+        res["e2e_pipelined"] = False
         res["h2d"] = h_in.numel() * h_in.element_size()
         res["d2h"] = h_out.numel() * h_out.element_size()
+        if flush is None:
+            # the same steps pipelined over a second set of input and output
+            # buffers (and a graph of the step over them)
+            io_in2, io_out2 = stage_io(layers, dev)
+            g_a2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_a2, stream=stream):
+                step()
+            with torch.cuda.stream(stream):
+                g_a2.replay()
+            torch.cuda.synchronize()
+            pip = time_pipelined([g_a, g_a2], [io_in, io_in2], [io_out, io_out2], h_in, h_out, stream,
+                                 args.steps, world, 5)
+            res["e2e_ms"] = max_over_ranks(statistics.median(pip), world)
+            res["e2e_pipelined"] = True
+            del g_a2, io_in2, io_out2
     if clocks is not None:
         res["clocks"] = clocks.stop()
     for L in layers:
@@ -728,6 +790,12 @@ def run_gpu(args) -> dict | None:
             "ms_per_step": round(head["e2e_ms"], 5),
             "h2d_bytes_per_step": head["h2d"],
             "d2h_bytes_per_step": head["d2h"],
+            "method": ("pipelined over two buffer sets: step i+1's inputs copied up and step i-1's "
+                       "outputs copied down while step i computes; every copy inside the timed region"
+                       if head["e2e_pipelined"] else
+                       "serial: upload, step, download and a host synchronize every step"),
+            "serial": {"value": round(whole_job(head["step_bytes"], world, head["e2e_serial_ms"]) / 1e9, 2),
+                       "ms_per_step": round(head["e2e_serial_ms"], 5)},
         },
         "gpu_launches": head["launches_per_step"] * args.steps * head["blocks"],
         "clocks": head["clocks"],
