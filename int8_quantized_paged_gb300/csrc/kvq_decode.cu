@@ -352,14 +352,14 @@ static kvq_status run_decode(const kvq_config* cfg, int32_t batch, const void* q
     // fragments, reused at the end for the warps' merge and then either the
     // cluster's partial or the combine's weights.
     const size_t ring_cl = tc_ring_bytes(*cfg, true), ring = tc_ring_bytes(*cfg, false);
-    const size_t pre = tc_pre_bytes(hd, nt, ng);
+    const size_t pre_cl = tc_pre_bytes(hd, nt, ng, true), pre = tc_pre_bytes(hd, nt, ng, false);
     auto merge_bytes = [&](int warps) { return ((size_t)warps * G * (hd + 2) + G) * sizeof(float); };
     TcLaunchCfg lc{};
     lc.stream = stream;
     lc.pdl = pdl_enabled();
 
     int cb = 0, recv = 0;
-    if (chunk_tokens == 0 && pick_cluster(*cfg, batch, max_tokens, window, fn, ring_cl, pre, &lc, &cb, &recv)) {
+    if (chunk_tokens == 0 && pick_cluster(*cfg, batch, max_tokens, window, fn, ring_cl, pre_cl, &lc, &cb, &recv)) {
       t.cluster = lc.cluster;
       t.blocks_per_chunk = cb;
       t.recv_off = recv;
@@ -445,7 +445,7 @@ extern "C" int32_t kvq_decode_cluster_ctas(const kvq_config* cfg, int32_t batch,
   TcLaunchCfg lc{};
   int cb = 0, recv = 0;
   const bool on = pick_cluster(*cfg, batch, max_tokens, window, tc_launcher(*cfg), tc_ring_bytes(*cfg, true),
-                               tc_pre_bytes(cfg->head_dim, G > 4 ? 2 : 1, tc_ng(*cfg)), &lc, &cb, &recv);
+                               tc_pre_bytes(cfg->head_dim, G > 4 ? 2 : 1, tc_ng(*cfg), true), &lc, &cb, &recv);
   return on ? lc.cluster : 0;
 }
 

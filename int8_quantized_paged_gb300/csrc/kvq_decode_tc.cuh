@@ -123,8 +123,14 @@ __host__ __device__ constexpr int tc_qfrag_bytes(int hd, int nt) { return nt * h
 // ([nt][ng][4 heads]) and, for a fused append, the new K and V rows (up to
 // fp32) with the RoPE row of their position, then their quantized rows (code
 // rows up to 2 hd bytes (f16), parameter rows up to 64 bytes).
-__host__ __device__ constexpr int tc_pre_bytes(int hd, int nt, int ng) {
-  return tc_qfrag_bytes(hd, nt) + 4 * hd + 16 * nt * ng + 16 * hd + 128;
+// The affine-K q sums: [group][4 heads] floats (NT = 1), [group][8] (NT = 2),
+// or in the cluster mode, where several warps build the fragments,
+// [32-dim unit][4 heads].
+__host__ __device__ constexpr int tc_qsum_bytes(int hd, int nt, int ng, bool cl) {
+  return cl && hd > 16 * nt * ng ? hd : 16 * nt * ng;
+}
+__host__ __device__ constexpr int tc_pre_bytes(int hd, int nt, int ng, bool cl) {
+  return tc_qfrag_bytes(hd, nt) + 4 * hd + tc_qsum_bytes(hd, nt, ng, cl) + 16 * hd + 128;
 }
 
 // Fused append: quantizes the staged row (K rotated at its position) exactly
@@ -298,6 +304,17 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   // tig (and 4 + tig), and the P.V accumulators are one tile (NO = 1).
   constexpr bool MRG = NT == 2;
   constexpr int NO = MRG ? 1 : NT;
+  // Query fragments in units of 32 dims (one uint4 of a lane: k-steps 2u,
+  // 2u+1; CPU K chunks).  In the cluster mode (8 warps; the appenders are
+  // warps 6 and 7) four warps build them, unit u by warp owner(u), each with
+  // its own slice of the RoPE row (and, for affine K, per-unit q sums the
+  // readers add up per group); elsewhere warp 0 builds them all.  A NeoX
+  // pair (u, u + NU/2) stays with one warp.
+  constexpr int CPU = F16 ? 4 : (K8 ? 2 : 1);
+  constexpr int NU = KCH / CPU;
+  constexpr int NBLD = CL ? cmin(4, NU) : 1;
+  static_assert(KSTEPS / 2 == NU, "one uint4 of fragments a unit");
+  static_assert(NBLD == 1 || !MRG, "several builders only with one tile");
 
   const DecodeArgs& a = A.d;
   const int G = A.G;
@@ -313,15 +330,16 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   // waits for this grid to finish before it reads anything it writes.
   // EARLY: before its wait a thread reads only inputs the caller guarantees
   // that kernel does not write (lengths, positions, table, RoPE rows, pages).
-  // Warp 0, which needs q, waits for a whole-context decode once its page-id
-  // loads are issued and before it uses them (a CTA that starts while that
-  // kernel runs has its ids by the end of the wait; one that starts later
-  // loads q together with them), and for a ring or a window, whose page ids
-  // need the length first, once its first page copies are issued (measured
-  // faster there: 8.75 against 9.19 us per window layer).  The appender
-  // warps, which need the new rows, wait once their roles are known.  The
-  // other warps read nothing that kernel writes; they wait after the barrier
-  // that ends the prologue (past warp 0's wait), before any write.  A thread
+  // The fragment builders (warp 0; warps 0-3 in the cluster mode), which
+  // need q, wait for a whole-context decode once their page-id loads are
+  // issued and before they use them (a CTA that starts while that kernel runs
+  // has its ids by the end of the wait; one that starts later loads q
+  // together with them), and for a ring or a window, whose page ids need the
+  // length first, once their first page copies are issued (measured faster
+  // there: 8.75 against 9.19 us per window layer).  The appender warps, which
+  // need the new rows, wait once their roles are known.  The other warps
+  // read nothing that kernel writes; they wait after the barrier that ends
+  // the prologue (past the builders' waits), before any write.  A thread
   // triggers its dependents only after its own wait.
   auto wait_inputs = [&]() {
     tc::grid_dependency_wait();
@@ -329,21 +347,25 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   };
   if constexpr (!EARLY) wait_inputs();
 
-  // One round of independent loads: the length, (warp 0) this lane's raw q
+  // One round of independent loads: the length, (builders) this lane's raw q
   // elements (see the fragments below) and, for a whole-context decode, the
   // block-table entries of the warp's pages, which do not depend on the length.
   const int64_t obase = ((int64_t)b * a.n_heads + (int64_t)kvh * G) * HD;
   const int L = a.seq_lens[b];
   const int apos = a.app_pos ? a.app_pos[b] : -1;   // fused append: position of the new row
   float qv[NT][KCH][RUN];
-  auto load_q = [&]() {
+  const bool neox = a.rope == KVQ_ROPE_NEOX;
+  auto owner = [&](int u) { return (neox ? u % (NU / 2) : u) % NBLD; };   // builder of unit u
+  const bool builder = NBLD == 1 ? warp == 0 : warp < NBLD;
+  auto load_q = [&]() {   // this warp's units
     // column gid of the B fragments: head (gid / 2) mod G (NT = 1) or head
     // gid (MRG: both passes, zero for a column past the last head)
     const int hq = MRG ? gid : (gid >> 1) % G;
     if (!MRG || hq < G) {
 #pragma unroll
       for (int c = 0; c < KCH; ++c)
-        load_run<RUN>(a.q, a.act, obase + (int64_t)hq * HD + KDC * c + RUN * tig, qv[0][c]);
+        if (NBLD == 1 || owner(c / CPU) == warp)
+          load_run<RUN>(a.q, a.act, obase + (int64_t)hq * HD + KDC * c + RUN * tig, qv[0][c]);
     } else {
 #pragma unroll
       for (int c = 0; c < KCH; ++c)
@@ -351,7 +373,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
         for (int k = 0; k < RUN; ++k) qv[0][c][k] = 0.f;
     }
   };
-  if (!EARLY && warp == 0) load_q();
+  if (!EARLY && builder) load_q();
   const int CB = A.blocks_per_chunk;
   const int w = warp;
   const int32_t* bt = a.block_table + (int64_t)b * a.max_pages;
@@ -361,7 +383,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     const int blk = chunk * CB + w + NW * lane;
     if (blk < a.max_pages) ids = bt[blk];
   }
-  if (EARLY && warp == 0 && whole) {
+  if (EARLY && builder && whole) {
     wait_inputs();
     load_q();
   }
@@ -428,16 +450,29 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   const int64_t page_lane = vlane ? a.vl.page_bytes : a.kl.page_bytes;
   if (!whole && lane < n_local) ids = page_of(lane);
   ids = checked(ids, lane);
-  // Warp 0 copies the RoPE row of position L - 1 into shared memory ahead of
-  // every page copy (as its own, oldest commit group), so the row does not
-  // queue behind the pages and the query fragments are ready before they are.
+  // The builders copy the RoPE row of position L - 1 into shared memory ahead
+  // of every page copy (each its units' part, as its own oldest commit group),
+  // so the row does not queue behind the pages and the query fragments are
+  // ready before they are.
   const uint32_t qfs = tc::smem_u32(smem) + (uint32_t)(NW * D * SLOT);   // fragments
   const uint32_t rope_s = qfs + tc_qfrag_bytes(HD, NT);                  // RoPE row
   const uint32_t qsum_s = rope_s + 4 * HD;                                // affine-K q sums
-  if (warp == 0 && a.rope != KVQ_ROPE_NONE) {
+  if (builder && a.rope != KVQ_ROPE_NONE) {
     const uint8_t* row = reinterpret_cast<const uint8_t*>(a.rope_tab) + (int64_t)(L - 1) * (4 * HD);
-    for (int j = lane; j < HD / 4; j += 32)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(rope_s + 16 * j), "l"(row + 16 * j) : "memory");
+    if (NBLD == 1) {
+      for (int j = lane; j < HD / 4; j += 32)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(rope_s + 16 * j), "l"(row + 16 * j) : "memory");
+    } else {
+      // unit u's entries: bytes [128 u, 128 u + 128) (pairs inside the unit's
+      // dims), or for NeoX [256 u, 256 u + 256) for u < NU / 2
+      const int ub = neox ? 256 : 128;
+#pragma unroll
+      for (int u = 0; u < NU; ++u)
+        if ((!neox || u < NU / 2) && owner(u) == warp && lane < ub / 16)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(rope_s + ub * u + 16 * lane),
+                       "l"(row + ub * u + 16 * lane)
+                       : "memory");
+    }
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
 
@@ -453,7 +488,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
   // warp that reads the page copies the buffers over the row's stale copy in
   // its slot when it gets there (after the barrier that ends the prologue),
   // so no read of the pool waits for the write.
-  const int app_off = NW * D * SLOT + tc_qfrag_bytes(HD, NT) + 4 * HD + 16 * NT * NG;   // [K][V][RoPE]
+  const int app_off = NW * D * SLOT + tc_qfrag_bytes(HD, NT) + 4 * HD + tc_qsum_bytes(HD, NT, NG, CL);   // [K][V][RoPE]
   int k_app = -1;    // the page warp: its page index of the new row
   int app_role = 0;  // 1: this warp quantizes the K row, 2: the V row
   int app_pg = -1;   // page id of the new row's block
@@ -568,41 +603,33 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
                        : "memory");
     }
   };
-  // Cluster mode at head_dim 256, whole context, early reads: the pages wait
-  // for warp 0's q and RoPE requests, which would otherwise queue behind the
-  // prologue's page burst (3 pages of 4.6 KB a warp on 96 SMs, about 1.6 us
-  // of HBM time).  The cluster's CTAs do not start before the previous
-  // kernel ends (its clusters hold the SMs), so holding the pages back costs
-  // no overlap.  Measured per global layer 24.7 -> 24.0-24.3 us; at head_dim 128
-  // (a 6.7 MB burst) the same barrier cost llama8b 8.29 -> 8.55 us.
-  if constexpr (CL && EARLY && HD == 256) {
-    if (whole) __syncthreads();
-  }
 #pragma unroll
   for (int k = 0; k < D; ++k) {
     if (k < n_local) issue(k, k);
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  if (EARLY && warp == 0 && !whole) {
+  if (EARLY && builder && !whole) {
     wait_inputs();
     load_q();
   }
 
-  // ---- query fragments (warp 0).  Lane (gid, tig) holds, for column gid
+  // ---- query fragments (the builders).  Lane (gid, tig) holds, for column gid
   // (head hq = gid / 2, part gid % 2), the q elements its K k-steps meet: the
   // runs of RUN dims starting at KDC*c + RUN*tig of every K chunk c.  They are
-  // the same for every warp of the CTA, so warp 0 keeps them in shared memory,
-  // [uint4 i][lane] with uint4 i = words of k-steps 2i, 2i+1, and every warp
-  // reloads the ones it needs per page (fewer live registers).
-  if (warp == 0) {
+  // the same for every warp of the CTA, so the builders keep them in shared
+  // memory, [uint4 i][lane] with uint4 i = words of k-steps 2i, 2i+1 (unit i),
+  // and every warp reloads the ones it needs per page (fewer live registers).
+  if (builder) {
     // the RoPE row: the oldest of this lane's D + 1 commit groups
     asm volatile("cp.async.wait_group %0;" ::"n"(D) : "memory");
     __syncwarp();
     const float sc = a.score_scale * kQScale;
     const int rope = a.rope;
+    auto mine = [&](int c) { return NBLD == 1 || owner(c / CPU) == warp; };   // chunk c is this warp's
     if (rope == KVQ_ROPE_NORMAL) {   // pairs (2i, 2i+1) lie inside a run
 #pragma unroll
       for (int c = 0; c < KCH; ++c)
+        if (mine(c))
 #pragma unroll
         for (int k = 0; k < RUN; k += 2) {
           float2 t;
@@ -615,6 +642,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     } else if (rope == KVQ_ROPE_NEOX) {   // pairs (i, i + HD/2): chunk c with chunk c + KCH/2
 #pragma unroll
       for (int c = 0; c < KCH / 2; ++c)
+        if (mine(c))
 #pragma unroll
         for (int k = 0; k < RUN; ++k) {
           float2 t;
@@ -627,6 +655,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     }
 #pragma unroll
     for (int c = 0; c < KCH; ++c)
+      if (mine(c))
 #pragma unroll
       for (int k = 0; k < RUN; ++k) qv[0][c][k] *= sc;
     // B fragments of tile (NT = 1) or pass (MRG) nt: 4-bit K chunk c, parity p
@@ -645,6 +674,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       uint32_t qb[KSTEPS][2];
 #pragma unroll
       for (int c = 0; c < KCH; ++c) {
+        if (!mine(c)) continue;
         if constexpr (F16) {
           qb[c / 2][c & 1] = tc::pack_half2(qp(qv[0][c][0]), qp(qv[0][c][1]));
         } else if constexpr (K8) {
@@ -661,13 +691,30 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
       }
 #pragma unroll
       for (int i = 0; i < KSTEPS / 2; ++i)
+        if (NBLD == 1 || owner(i) == warp)
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qfs + ((nt * (KSTEPS / 2) + i) * 32 + lane) * 16),
                      "r"(qb[2 * i][0]), "r"(qb[2 * i][1]), "r"(qb[2 * i + 1][0]), "r"(qb[2 * i + 1][1])
                      : "memory");
     }
     // affine K: per-group q sums of the columns' heads: [g][4] at lane 8h for
-    // head h (gid = 2h, NT = 1), [g][8] at lane 4h for head h (MRG)
-    if constexpr (KAFF) {
+    // head h (gid = 2h, NT = 1), [g][8] at lane 4h for head h (MRG); with
+    // several builders, per-unit sums [u][4], which the readers add per group
+    if constexpr (KAFF && NBLD > 1) {
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        if (owner(u) != warp) continue;
+        float v = 0.f;
+#pragma unroll
+        for (int c = u * CPU; c < (u + 1) * CPU; ++c)
+#pragma unroll
+          for (int k = 0; k < RUN; ++k) v += qv[0][c][k];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (tig == 0 && (gid & 1) == 0)
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(qsum_s + 4 * (u * 4 + (gid >> 1))), "f"(v * (1.0f / kQScale))
+                       : "memory");
+      }
+    } else if constexpr (KAFF) {
       float part_sum[KNG];
 #pragma unroll
       for (int g = 0; g < KNG; ++g) part_sum[g] = 0.f;
@@ -693,7 +740,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     }
   }
   // The new row is quantized now, while the pages are still arriving, by the
-  // two appender warps in parallel with warp 0's fragments; the barrier below
+  // two appender warps in parallel with the builders' fragments; the barrier below
   // publishes the row buffers to the page warp.
   if (app_role != 0) {
     asm volatile("cp.async.wait_group %0;" ::"n"(D) : "memory");   // the staged row: older than the pages
@@ -702,7 +749,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
     __syncwarp();
   }
   __syncthreads();
-  if (EARLY && warp != 0 && app_role == 0) wait_inputs();
+  if (EARLY && !builder && app_role == 0) wait_inputs();
   // affine K: the q sums of this lane's score heads: tig (mod G) for NT = 1,
   // 2 tig + h2 for head slot h2 (MRG)
   float qsum[NT][KNG];
@@ -711,7 +758,14 @@ decode_tc_kernel(const __grid_constant__ TcArgs A) {
 #pragma unroll
     for (int g = 0; g < KNG; ++g) {
       qsum[nt][g] = 0.f;
-      if constexpr (KAFF) {
+      if constexpr (KAFF && NBLD > 1) {   // the group's units: GS / 32 of them
+#pragma unroll
+        for (int u = g * (GS / 32); u < (g + 1) * (GS / 32); ++u) {
+          float x;
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(x) : "r"(qsum_s + 4 * (u * 4 + tig % G)) : "memory");
+          qsum[nt][g] += x;
+        }
+      } else if constexpr (KAFF) {
         const int slot = MRG ? g * 8 + 2 * tig + nt : g * 4 + tig % G;
         asm volatile("ld.shared.f32 %0, [%1];" : "=f"(qsum[nt][g]) : "r"(qsum_s + 4 * slot) : "memory");
       }

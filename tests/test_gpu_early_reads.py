@@ -41,8 +41,8 @@ CASES = {
     "llama8b_b3": dict(name="llama8b", lens=[1000, 33, 2049], over=dict(batch=3), chain_kv=False),
     "long_mixed": dict(name="long_mixed", lens=[5000, 777], over=dict(batch=2), chain_kv=False),
     "gemma_window": dict(name="gemma_mix", lens=[3001], ring=1152, window=1024, chain_kv=True),
-    # head_dim 256, whole context: the cluster CTAs hold their page copies at a
-    # block barrier until warp 0 has issued its q and RoPE requests
+    # head_dim 256, whole context, affine K: four warps of each cluster CTA
+    # build the query fragments and per-unit q sums after their waits
     "gemma_global": dict(name="gemma_mix", lens=[3001], chain_kv=True),
 }
 
