@@ -71,7 +71,12 @@
 extern "C" {
 #endif
 
-#define KVQ_ABI_VERSION 1
+/* 1: the first release.  2: kvq_config.flags (formerly a reserved field
+ * that had to be 0) accepts KVQ_FLAG_EARLY_READS; a caller that sets it can
+ * check kvq_abi_version() >= 2 first, as a version-1 library refuses any
+ * nonzero value with KVQ_ERR_INVALID_ARG.  The layout of every struct is
+ * unchanged. */
+#define KVQ_ABI_VERSION 2
 
 /* A cudaStream_t.  NULL means the legacy default stream. */
 typedef struct CUstream_st* kvq_stream_t;
