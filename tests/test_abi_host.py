@@ -265,3 +265,24 @@ def test_pool_finalized_before_its_table_is_safe():
         cycle.append(cycle)           # a reference cycle the collector has to break
         del cycle
         gc.collect()
+
+
+@pytest.mark.parametrize("name", ["kvq_append", "kvq_decode_attention", "kvq_decode_attention_noalloc",
+                                  "kvq_window_decode", "kvq_append_decode_attention",
+                                  "kvq_append_window_decode"])
+def test_unknown_flag_bits_refused_by_every_entry_point(name):
+    """An unknown kvq_config.flags bit fails the host checks of every device
+    entry point before any pointer is touched or anything is launched."""
+    c = _cfg(wl.workload("llama8b"))
+    c.flags = 1 << 4
+    fn = getattr(kvq.lib(), name)
+    args = []
+    for t in fn.argtypes:
+        if t is C.c_void_p:
+            args.append(None)
+        elif t in (C.c_int32, C.c_int64, C.c_size_t):
+            args.append(1)
+        else:                               # the config pointer
+            args.append(C.byref(c))
+    assert fn(*args) == kvq.ERR_INVALID_ARG
+    assert "flags" in kvq.last_error()
